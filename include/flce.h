@@ -1,0 +1,181 @@
+/*
+ * flce.h - C ABI of the fused linear cross-entropy library for GB300 (sm_103a).
+ *
+ * The operation (source: "Long-Sequence MoE RL Training: From First Principles
+ * to MI300X", section 3 "Linear cross-entropy: don't build a 32 GB tensor to
+ * get a scalar"): the language-model head forms logits Z = H W^T over
+ * [tokens x vocab] and reduces every row through the softmax to a per-token
+ * cross-entropy.  The fused method never stores Z: it tiles the token axis,
+ * forms each logit tile on the fly and folds it into a running maximum and
+ * log-sum-exp, keeping only a few scalars per row.  The backward recomputes
+ * each logit tile, forms dZ = softmax(Z) - onehot(target) (scaled by the
+ * upstream per-token gradient) and contracts it at once into dH = dZ W and
+ * dW = dZ^T H, so only a [block x vocab] slice of dZ is ever resident.
+ * Section 2.3, Step 1 of "让长序列 MoE RL 训练更好调：Megatron-Lite / bumblebee
+ * 的优化实践" describes the same loss as streaming along the vocab dimension.
+ *
+ * Notation: T tokens, Hd hidden size, V vocabulary size.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device and
+ *     stay owned by the caller.  The library never allocates device memory:
+ *     the caller passes a workspace of at least the size the matching
+ *     *_workspace_size() function returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL means the legacy default stream).  Outputs are overwritten, never
+ *     accumulated into.
+ *   - Argument errors are detected on the host and returned before anything
+ *     is launched.  Errors that depend on device data (a target outside
+ *     [0, V) that is not ignore_index; a bounded wait inside a kernel that
+ *     ran out) are written to a status word at the start of the workspace;
+ *     read it with flce_read_device_status().  Each call clears that word
+ *     first, so it reports the latest call made with this workspace.  Rows
+ *     whose target is out of range are treated as ignored.
+ *   - H and W are bf16, row-major: H [T, Hd], W [V, Hd], each row contiguous.
+ *     Hd must be a positive multiple of 64; H, W, dH and dW must be 16-byte
+ *     aligned; the workspace 256-byte aligned.  T may be 0.  V >= 1.
+ *     T, V < 2^31.
+ *   - Rows whose target equals ignore_index contribute zero loss and zero
+ *     gradient and are not counted in n_valid.  ignore_index must lie outside
+ *     [0, V).
+ *   - Reductions: MEAN = sum over valid rows / n_valid (0 when n_valid == 0),
+ *     SUM = sum over valid rows, NONE = one loss per token.
+ *   - Results are deterministic: the same inputs and workspace size give
+ *     bit-identical outputs on the same device.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FLCE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FLCE_API __attribute__((visibility("default")))
+#else
+#define FLCE_API
+#endif
+
+typedef enum flce_status {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad reduction, ignore_index in [0, V) */
+  FLCE_ERR_UNSUPPORTED = 2,  /* Hd not a multiple of 64, or the device is not sm_103 */
+  FLCE_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned (workspace: 256) */
+  FLCE_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+  FLCE_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed; see flce_last_error() */
+  FLCE_ERR_TARGET_RANGE = 6, /* device status: a target outside [0, V) and != ignore_index */
+  FLCE_ERR_TIMEOUT = 7       /* device status: a bounded wait inside a kernel ran out */
+} flce_status;
+
+typedef enum flce_reduction {
+  FLCE_REDUCTION_NONE = 0,
+  FLCE_REDUCTION_MEAN = 1,
+  FLCE_REDUCTION_SUM = 2
+} flce_reduction;
+
+/* Bytes of workspace flce_forward() needs for these sizes (>= 256). */
+FLCE_API size_t flce_forward_workspace_size(int64_t T, int64_t Hd, int64_t V);
+
+/* Bytes of workspace flce_backward() needs to run with its default token
+ * chunk.  The backward works on token chunks of `chunk` rows; the workspace
+ * holds one [chunk x V] bf16 slice of dZ (the page's [block x vocab]
+ * residency) plus O(T) scalars.  The default chunk is below T whenever
+ * T > 256, so the workspace stays below the T*V*2 bytes of one dense bf16
+ * logits tensor.  A larger or smaller workspace is accepted: the backward then
+ * uses the largest chunk (a multiple of 128 tokens, at least 128) that fits. */
+FLCE_API size_t flce_backward_workspace_size(int64_t T, int64_t Hd, int64_t V);
+
+/* The token chunk flce_backward() uses with a workspace of `workspace_bytes`;
+ * 0 if the workspace is too small. */
+FLCE_API int64_t flce_backward_chunk_tokens(int64_t T, int64_t Hd, int64_t V, size_t workspace_bytes);
+
+/* Forward.  Source: section 3 of the first page (logits H W^T reduced row-wise
+ * through the running-max / log-sum-exp recurrence; loss per token).
+ *   H        [T, Hd] bf16              hidden states
+ *   W        [V, Hd] bf16              LM-head weight
+ *   targets  [T] int64                 class per token, or ignore_index
+ *   loss     [1] fp32 (MEAN, SUM) or [T] fp32 (NONE)
+ *   lse      [T] fp32                  log sum_v exp(z_{t,v}) on every row
+ *   logp     [T] fp32                  z_{t,y_t} - lse_t; 0 on ignored rows
+ *   n_valid  [1] int64 or NULL         number of rows with a valid target
+ *   workspace, workspace_bytes         >= flce_forward_workspace_size(T, Hd, V)
+ * No [T x V] buffer exists at any time. */
+FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd,
+                                  int64_t V, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
+                                  float* logp, int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* Backward.  Source: section 3 of the first page (recompute the logit tile,
+ * form dZ = softmax - onehot for it, contract it into dH and dW at once).
+ *   dloss    [1] fp32 (MEAN, SUM) or [T] fp32 (NONE): gradient of the loss output
+ *   H, W, targets, T, Hd, V, ignore_index, reduction: as passed to flce_forward
+ *   lse      [T] fp32                  the lse output of flce_forward for these inputs
+ *   dH       [T, Hd] bf16              overwritten with dL/dH (fp32 accumulation, rounded)
+ *   dW       [V, Hd] fp32              overwritten with dL/dW, accumulated in fp32 over
+ *                                      token chunks in a fixed order
+ *   workspace, workspace_bytes         see flce_backward_workspace_size()
+ * Per token, the upstream weight is g_t = dloss/n_valid (MEAN), dloss (SUM) or
+ * dloss[t] (NONE), and 0 on ignored rows; dZ_{t,v} = g_t (exp(z_{t,v} - lse_t) - [v = y_t]). */
+FLCE_API flce_status flce_backward(const float* dloss, const void* H, const void* W, const int64_t* targets,
+                                   const float* lse, int64_t T, int64_t Hd, int64_t V, int64_t ignore_index,
+                                   int32_t reduction, void* dH, float* dW, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Synchronizes `stream`, then reads the device status word of the latest call
+ * made with `workspace` into *out (an flce_status value). */
+FLCE_API flce_status flce_read_device_status(const void* workspace, void* stream, int32_t* out);
+
+/* Human-readable name of a status code (static storage). */
+FLCE_API const char* flce_status_string(int32_t status);
+
+/* Text of the last FLCE_ERR_CUDA / argument error raised on this host thread. */
+FLCE_API const char* flce_last_error(void);
+
+/* FLCE_ABI_VERSION of the loaded library. */
+FLCE_API int32_t flce_abi_version(void);
+
+/* Limit, in nanoseconds, of every bounded wait inside the kernels (default
+ * 4e9).  Values below 1e6 are raised to 1e6.  Affects later launches only. */
+FLCE_API void flce_set_wait_timeout_ns(uint64_t ns);
+
+/* ---- per-kernel timing, a profiling aid ------------------------------------
+ * While enabled, every kernel launch of the library is bracketed by CUDA
+ * events recorded on its launch stream.  flce_profile_collect() synchronizes
+ * on those events and returns, per kernel kind, the launches, the summed
+ * device time and the summed algorithmic work (FLOPs and bytes the kernel's
+ * mathematics requires, independent of how it is executed). */
+typedef struct flce_kernel_stats {
+  int32_t kind;     /* flce_kernel_kind value */
+  int32_t launches;
+  double total_ms;
+  double flops;     /* algorithmic FLOPs summed over the launches */
+  double bytes;     /* algorithmic DRAM bytes summed over the launches */
+} flce_kernel_stats;
+
+typedef enum flce_kernel_kind {
+  FLCE_KERNEL_FWD_LOGITS_LSE = 0, /* logit tiles H W^T + running max / sum-exp epilogue */
+  FLCE_KERNEL_FWD_FINALIZE = 1,   /* per-row lse / loss / logp and block partial sums */
+  FLCE_KERNEL_FWD_REDUCE = 2,     /* fixed-order scalar loss and n_valid */
+  FLCE_KERNEL_BWD_PREP = 3,       /* n_valid and the per-token upstream weights g */
+  FLCE_KERNEL_BWD_DZ = 4,         /* recomputed logit tiles + dZ epilogue, bf16 dZ chunk */
+  FLCE_KERNEL_BWD_DH = 5,         /* dH chunk = dZ W */
+  FLCE_KERNEL_BWD_DW = 6,         /* dW += dZ^T H for one chunk */
+  FLCE_KERNEL_KINDS = 7
+} flce_kernel_kind;
+
+FLCE_API void flce_profile_enable(int32_t on);
+/* Fills up to `max_entries` records (one per kind that launched), sets *n_out,
+ * and clears the records.  Returns FLCE_ERR_CUDA if an event query fails. */
+FLCE_API flce_status flce_profile_collect(flce_kernel_stats* out, int32_t max_entries, int32_t* n_out);
+FLCE_API const char* flce_kernel_name(int32_t kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

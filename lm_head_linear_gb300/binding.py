@@ -1,0 +1,257 @@
+"""ctypes binding of ``libflce.so`` (the C ABI in ``include/flce.h``).
+
+Argument marshalling only: tensors are checked, output / workspace buffers are
+allocated with torch (device-memory plumbing), and every step of the
+computation runs in the library's CUDA kernels.  There is no CPU or PyTorch
+fallback: if the library is missing or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+REDUCTIONS = {"none": 0, "mean": 1, "sum": 2}
+STATUS_NAMES = {
+    0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_ALIGNMENT",
+    4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
+}
+KERNEL_KINDS = 7
+
+# Every symbol the header declares: name -> (restype, argtypes).
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+SIGNATURES = {
+    "flce_forward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "flce_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "flce_backward_chunk_tokens": (_I64, [_I64, _I64, _I64, ctypes.c_size_t]),
+    "flce_forward": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_backward": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
+    "flce_status_string": (ctypes.c_char_p, [_I32]),
+    "flce_last_error": (ctypes.c_char_p, []),
+    "flce_abi_version": (_I32, []),
+    "flce_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "flce_profile_enable": (None, [_I32]),
+    "flce_profile_collect": (_I32, [_P, _I32, ctypes.POINTER(_I32)]),
+    "flce_kernel_name": (ctypes.c_char_p, [_I32]),
+}
+
+
+class KernelStats(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+class FlceError(RuntimeError):
+    def __init__(self, status: int, detail: str = ""):
+        self.status = int(status)
+        super().__init__(f"{STATUS_NAMES.get(self.status, self.status)}: {detail}")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the in-tree library (raises if it was not built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m lm_head_linear_gb300.build` "
+                               "(there is no fallback implementation)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if lib.flce_abi_version() != 1:
+            raise RuntimeError("libflce ABI version mismatch")
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load_library()
+        raise FlceError(status, (lib.flce_last_error() or b"").decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_inputs(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor):
+    if not (H.is_cuda and W.is_cuda and targets.is_cuda):
+        raise ValueError("H, W and targets must be CUDA tensors")
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("H and W must be bfloat16")
+    if targets.dtype != torch.int64:
+        raise ValueError("targets must be int64")
+    if H.dim() != 2 or W.dim() != 2 or targets.dim() != 1:
+        raise ValueError("H [T, Hd], W [V, Hd], targets [T]")
+    if H.shape[1] != W.shape[1] or H.shape[0] != targets.shape[0]:
+        raise ValueError(f"shape mismatch: H {tuple(H.shape)}, W {tuple(W.shape)}, targets {tuple(targets.shape)}")
+    if not (H.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
+        raise ValueError("H, W and targets must be contiguous")
+
+
+def flce_forward_workspace_size(T: int, Hd: int, V: int) -> int:
+    return int(load_library().flce_forward_workspace_size(T, Hd, V))
+
+
+def flce_backward_workspace_size(T: int, Hd: int, V: int) -> int:
+    return int(load_library().flce_backward_workspace_size(T, Hd, V))
+
+
+def flce_backward_chunk_tokens(T: int, Hd: int, V: int, workspace_bytes: int) -> int:
+    return int(load_library().flce_backward_chunk_tokens(T, Hd, V, workspace_bytes))
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def flce_forward(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+                 reduction: str = "mean", workspace: Optional[torch.Tensor] = None, stream=None,
+                 out: Optional[dict] = None):
+    """Run ``flce_forward``; returns ``(loss, lse, logp, n_valid, workspace)``.
+
+    ``loss`` is a 1-element fp32 tensor (mean / sum) or [T] (none); ``n_valid``
+    a 1-element int64 tensor.  ``out`` may hold preallocated ``loss``, ``lse``,
+    ``logp`` and ``n_valid`` tensors.
+    """
+    _check_inputs(H, W, targets)
+    lib = load_library()
+    T, Hd = H.shape
+    V = W.shape[0]
+    red = REDUCTIONS[reduction]
+    dev = H.device
+    out = out or {}
+    loss = out.get("loss")
+    if loss is None:
+        loss = torch.empty(T if red == 0 else 1, dtype=torch.float32, device=dev)
+    lse = out.get("lse")
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+    logp = out.get("logp")
+    if logp is None:
+        logp = torch.empty(T, dtype=torch.float32, device=dev)
+    n_valid = out.get("n_valid")
+    if n_valid is None:
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    need = lib.flce_forward_workspace_size(T, Hd, V)
+    ws = _workspace(need, dev, workspace)
+    st = lib.flce_forward(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), red, _ptr(loss), _ptr(lse),
+                          _ptr(logp), _ptr(n_valid), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _check(st)
+    return loss, lse, logp, n_valid, ws
+
+
+def flce_backward(dloss: torch.Tensor, H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                  ignore_index: int = -100, reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
+                  stream=None, out: Optional[dict] = None):
+    """Run ``flce_backward``; returns ``(dH bf16 [T, Hd], dW fp32 [V, Hd], workspace)``."""
+    _check_inputs(H, W, targets)
+    lib = load_library()
+    T, Hd = H.shape
+    V = W.shape[0]
+    red = REDUCTIONS[reduction]
+    dev = H.device
+    dloss = dloss.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
+    if dloss.numel() != (T if red == 0 else 1):
+        raise ValueError("dloss must have one element (mean / sum) or T elements (none)")
+    lse = lse.contiguous()
+    out = out or {}
+    dH = out.get("dH")
+    if dH is None:
+        dH = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
+    dW = out.get("dW")
+    if dW is None:
+        dW = torch.empty((V, Hd), dtype=torch.float32, device=dev)
+    need = lib.flce_backward_workspace_size(T, Hd, V)
+    ws = _workspace(need, dev, workspace)
+    st = lib.flce_backward(_ptr(dloss), _ptr(H), _ptr(W), _ptr(targets), _ptr(lse), T, Hd, V, int(ignore_index),
+                           red, _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _check(st)
+    return dH, dW, ws
+
+
+def flce_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    lib = load_library()
+    v = ctypes.c_int32(-1)
+    _check(lib.flce_read_device_status(_ptr(workspace), _stream_handle(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def flce_set_wait_timeout_ns(ns: int):
+    load_library().flce_set_wait_timeout_ns(int(ns))
+
+
+def flce_profile_enable(on: bool = True):
+    load_library().flce_profile_enable(1 if on else 0)
+
+
+def flce_profile_collect() -> dict:
+    """Per-kernel-kind {name: {launches, total_ms, flops, bytes}} since the last collect."""
+    lib = load_library()
+    arr = (KernelStats * KERNEL_KINDS)()
+    n = ctypes.c_int32(0)
+    _check(lib.flce_profile_collect(ctypes.cast(arr, ctypes.c_void_p), KERNEL_KINDS, ctypes.byref(n)))
+    res = {}
+    for i in range(n.value):
+        r = arr[i]
+        res[lib.flce_kernel_name(r.kind).decode()] = {
+            "launches": int(r.launches), "total_ms": float(r.total_ms), "flops": float(r.flops),
+            "bytes": float(r.bytes)}
+    return res
+
+
+class LinearCrossEntropy(torch.autograd.Function):
+    """autograd wrapper: forward runs ``flce_forward``, backward ``flce_backward``.
+
+    Returns ``(loss, logp)``; ``logp`` is an output only (no gradient flows
+    through it).  The weight gradient comes back in W's dtype.
+    """
+
+    @staticmethod
+    def forward(ctx, H, W, targets, ignore_index: int = -100, reduction: str = "mean"):
+        loss, lse, logp, _, _ = flce_forward(H, W, targets, ignore_index, reduction)
+        ctx.save_for_backward(H, W, targets, lse)
+        ctx.ignore_index = ignore_index
+        ctx.reduction = reduction
+        ctx.mark_non_differentiable(logp)
+        if reduction != "none":
+            loss = loss.reshape(())
+        return loss, logp
+
+    @staticmethod
+    def backward(ctx, dloss, dlogp):
+        H, W, targets, lse = ctx.saved_tensors
+        if dloss is None:
+            dloss = torch.zeros(1 if ctx.reduction != "none" else H.shape[0], device=H.device)
+        dH, dW, _ = flce_backward(dloss, H, W, targets, lse, ctx.ignore_index, ctx.reduction)
+        return dH, dW.to(W.dtype), None, None, None
+
+
+def linear_cross_entropy(H, W, targets, ignore_index: int = -100, reduction: str = "mean"):
+    """Fused ``cross_entropy(H @ W.T, targets)`` without materialising the logits; returns the loss."""
+    return LinearCrossEntropy.apply(H, W, targets, ignore_index, reduction)[0]

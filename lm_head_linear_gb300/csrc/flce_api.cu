@@ -1,0 +1,589 @@
+// Host side of the C ABI declared in include/flce.h: argument checks, workspace
+// layout, TMA tensor maps, launch sequence and the optional per-kernel timing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "flce.h"
+#include "flce_kernels.cuh"
+
+namespace {
+
+using namespace flce;
+
+thread_local char g_last_error[512] = "";
+
+flce_status fail(flce_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                            \
+  do {                                                                                            \
+    cudaError_t e_ = (expr);                                                                      \
+    if (e_ != cudaSuccess) return fail(FLCE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));  \
+  } while (0)
+
+constexpr size_t kHeaderBytes = 256;  // status word and spare scalars at the start of each workspace
+constexpr int kMaxSplit = 16;         // forward: vocab ranges per token block
+constexpr int64_t kDefaultChunk = 8192;
+
+uint64_t g_timeout_ns = 4000000000ull;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ device info
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  bool attrs_set = false;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+flce_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(FLCE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    CUDA_TRY(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev));
+    d.init = true;
+  }
+  if (!(d.major == 10 && d.minor == 3))
+    return fail(FLCE_ERR_UNSUPPORTED, "this library is built for sm_103a; device is sm_%d%d", d.major, d.minor);
+  if (!d.attrs_set) {
+    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_FWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_bytes_for(MODE_FWD)));
+    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_bytes_for(MODE_DZ)));
+    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_bytes_for(MODE_DH)));
+    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_bytes_for(MODE_DW)));
+    d.attrs_set = true;
+  }
+  *out = &d;
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+flce_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return FLCE_OK;
+}
+
+// 2-D map over a row-major matrix: `inner` contiguous elements per row,
+// `outer` rows, `pitch` bytes between rows; box {box_inner, box_outer};
+// 128-byte swizzle; out-of-range elements read as zero, stores are clipped.
+flce_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+                     uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for dims {%llu, %llu} pitch %llu box {%u, %u}",
+                static_cast<int>(r), static_cast<unsigned long long>(inner), static_cast<unsigned long long>(outer),
+                static_cast<unsigned long long>(pitch), box_inner, box_outer);
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------------ profiling
+struct LaunchRecord {
+  int kind;
+  cudaEvent_t start, stop;
+  double flops, bytes;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<LaunchRecord> g_records;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one launch with events on its stream while profiling is enabled.
+struct KernelScope {
+  bool on = false;
+  LaunchRecord rec{};
+  cudaStream_t stream;
+  KernelScope(int kind, cudaStream_t s, double flops, double bytes) : stream(s) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    on = true;
+    rec.kind = kind;
+    rec.flops = flops;
+    rec.bytes = bytes;
+    rec.start = take_event();
+    rec.stop = take_event();
+    cudaEventRecord(rec.start, s);
+  }
+  void done() {
+    if (!on) return;
+    cudaEventRecord(rec.stop, stream);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_records.push_back(rec);
+    on = false;
+  }
+};
+
+flce_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FLCE_ERR_CUDA, "launch of %s failed: %s", what, cudaGetErrorString(e));
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------------ workspace layouts
+struct FwdLayout {
+  int n_split;
+  int64_t part_stride;
+  size_t partials_off, zy_off, bsum_off, bcnt_off, total;
+  int num_fin_blocks;
+};
+
+FwdLayout fwd_layout(int64_t T, int n_split) {
+  FwdLayout L{};
+  L.n_split = n_split;
+  L.part_stride = static_cast<int64_t>(align_up(static_cast<size_t>(std::max<int64_t>(T, 1)), 128));
+  L.num_fin_blocks = static_cast<int>(std::max<int64_t>(cdiv(T, kFinalizeThreads), 1));
+  size_t off = kHeaderBytes;
+  L.partials_off = off;
+  off = align_up(off + sizeof(float2) * static_cast<size_t>(n_split) * L.part_stride, 256);
+  L.zy_off = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(L.part_stride), 256);
+  L.bsum_off = off;
+  off = align_up(off + sizeof(double) * L.num_fin_blocks, 256);
+  L.bcnt_off = off;
+  off = align_up(off + sizeof(int64_t) * L.num_fin_blocks, 256);
+  L.total = off;
+  return L;
+}
+
+struct BwdLayout {
+  int64_t chunk;
+  int64_t v_pad;
+  size_t g_off, dz_off, total;
+};
+
+BwdLayout bwd_layout(int64_t T, int64_t V, int64_t chunk) {
+  BwdLayout L{};
+  L.chunk = chunk;
+  L.v_pad = static_cast<int64_t>(align_up(static_cast<size_t>(V), 64));
+  size_t off = kHeaderBytes;
+  L.g_off = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(std::max<int64_t>(T, 1)), 1024);
+  L.dz_off = off;
+  off = align_up(off + 2ull * static_cast<size_t>(chunk) * L.v_pad, 256);
+  L.total = off;
+  return L;
+}
+
+int64_t default_chunk(int64_t T) {
+  // Below T whenever T > 256, so dZ residency stays [chunk x V] < [T x V].
+  int64_t c = static_cast<int64_t>(align_up(static_cast<size_t>(cdiv(std::max<int64_t>(T, 1), 2)), 128));
+  c = std::max<int64_t>(c, 128);
+  return std::min<int64_t>(c, kDefaultChunk);
+}
+
+// Vocab ranges per token block for the forward: the count whose units spread
+// most evenly over `grid` persistent CTAs (ties go to fewer ranges).
+int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
+  int best = 1;
+  double best_eff = -1.0;
+  const int max_split = static_cast<int>(std::min<int64_t>(kMaxSplit, n_blocks));
+  for (int ns = 1; ns <= max_split; ++ns) {
+    const int64_t units = m_blocks * ns;
+    const int64_t per_unit = cdiv(n_blocks, ns);
+    const int64_t waves = cdiv(units, grid);
+    const double eff = static_cast<double>(m_blocks * n_blocks) /
+                       static_cast<double>(std::min<int64_t>(units, grid) * waves * per_unit);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+flce_status check_common(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
+                         int64_t ignore_index, int32_t reduction) {
+  if (T < 0 || T >= (int64_t(1) << 31)) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
+  if (V < 1 || V >= (int64_t(1) << 31)) return fail(FLCE_ERR_INVALID_ARG, "V = %lld out of range", (long long)V);
+  if (Hd < 1 || Hd >= (int64_t(1) << 24)) return fail(FLCE_ERR_INVALID_ARG, "Hd = %lld out of range", (long long)Hd);
+  if (Hd % 64 != 0) return fail(FLCE_ERR_UNSUPPORTED, "Hd = %lld is not a multiple of 64", (long long)Hd);
+  if (reduction < 0 || reduction > 2) return fail(FLCE_ERR_INVALID_ARG, "unknown reduction %d", reduction);
+  if (ignore_index >= 0 && ignore_index < V)
+    return fail(FLCE_ERR_INVALID_ARG, "ignore_index %lld lies inside [0, V)", (long long)ignore_index);
+  if (!W) return fail(FLCE_ERR_INVALID_ARG, "W is NULL");
+  if (T > 0 && (!H || !targets)) return fail(FLCE_ERR_INVALID_ARG, "H or targets is NULL");
+  if ((reinterpret_cast<uintptr_t>(H) | reinterpret_cast<uintptr_t>(W)) & 15)
+    return fail(FLCE_ERR_ALIGNMENT, "H and W must be 16-byte aligned");
+  return FLCE_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+int32_t flce_abi_version(void) { return FLCE_ABI_VERSION; }
+
+const char* flce_last_error(void) { return g_last_error; }
+
+const char* flce_status_string(int32_t st) {
+  switch (st) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED";
+    case FLCE_ERR_ALIGNMENT: return "FLCE_ERR_ALIGNMENT";
+    case FLCE_ERR_WORKSPACE: return "FLCE_ERR_WORKSPACE";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+    case FLCE_ERR_TARGET_RANGE: return "FLCE_ERR_TARGET_RANGE";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+    default: return "FLCE_ERR_UNKNOWN";
+  }
+}
+
+void flce_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = std::max<uint64_t>(ns, 1000000ull); }
+
+const char* flce_kernel_name(int32_t kind) {
+  switch (kind) {
+    case FLCE_KERNEL_FWD_LOGITS_LSE: return "fwd_logits_lse";
+    case FLCE_KERNEL_FWD_FINALIZE: return "fwd_finalize";
+    case FLCE_KERNEL_FWD_REDUCE: return "fwd_reduce";
+    case FLCE_KERNEL_BWD_PREP: return "bwd_prep";
+    case FLCE_KERNEL_BWD_DZ: return "bwd_dz";
+    case FLCE_KERNEL_BWD_DH: return "bwd_dh";
+    case FLCE_KERNEL_BWD_DW: return "bwd_dw";
+    default: return "unknown";
+  }
+}
+
+void flce_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+flce_status flce_profile_collect(flce_kernel_stats* out, int32_t max_entries, int32_t* n_out) {
+  std::vector<LaunchRecord> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_records);
+  }
+  flce_kernel_stats agg[FLCE_KERNEL_KINDS];
+  for (int k = 0; k < FLCE_KERNEL_KINDS; ++k) agg[k] = flce_kernel_stats{k, 0, 0.0, 0.0, 0.0};
+  flce_status st = FLCE_OK;
+  for (auto& r : recs) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      st = fail(FLCE_ERR_CUDA, "event query failed");
+    agg[r.kind].launches += 1;
+    agg[r.kind].total_ms += ms;
+    agg[r.kind].flops += r.flops;
+    agg[r.kind].bytes += r.bytes;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& r : recs) {
+      g_event_pool.push_back(r.start);
+      g_event_pool.push_back(r.stop);
+    }
+  }
+  int n = 0;
+  for (int k = 0; k < FLCE_KERNEL_KINDS; ++k)
+    if (agg[k].launches > 0 && n < max_entries && out) out[n++] = agg[k];
+  if (n_out) *n_out = n;
+  return st;
+}
+
+size_t flce_forward_workspace_size(int64_t T, int64_t Hd, int64_t V) {
+  (void)Hd;
+  if (T < 0 || V < 1) return 0;
+  return fwd_layout(T, kMaxSplit).total;
+}
+
+size_t flce_backward_workspace_size(int64_t T, int64_t Hd, int64_t V) {
+  (void)Hd;
+  if (T < 0 || V < 1) return 0;
+  return bwd_layout(T, V, default_chunk(T)).total;
+}
+
+int64_t flce_backward_chunk_tokens(int64_t T, int64_t Hd, int64_t V, size_t workspace_bytes) {
+  (void)Hd;
+  if (T < 0 || V < 1) return 0;
+  const int64_t cap = static_cast<int64_t>(align_up(static_cast<size_t>(std::max<int64_t>(T, 1)), 128));
+  const BwdLayout L0 = bwd_layout(T, V, 0);
+  if (workspace_bytes < L0.total) return 0;
+  const size_t per_row = 2ull * static_cast<size_t>(L0.v_pad);
+  int64_t c = static_cast<int64_t>((workspace_bytes - L0.dz_off) / per_row);
+  c = c / 128 * 128;
+  c = std::min(c, cap);
+  return c < 128 ? 0 : c;
+}
+
+flce_status flce_read_device_status(const void* workspace, void* stream, int32_t* out) {
+  if (!workspace || !out) return fail(FLCE_ERR_INVALID_ARG, "workspace or out is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  CUDA_TRY(cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  *out = v;
+  return FLCE_OK;
+}
+
+flce_status flce_forward(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
+                         int64_t ignore_index, int32_t reduction, float* loss, float* lse, float* logp,
+                         int64_t* n_valid, void* workspace, size_t workspace_bytes, void* stream) {
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
+  if (st != FLCE_OK) return st;
+  if (!loss || (T > 0 && (!lse || !logp))) return fail(FLCE_ERR_INVALID_ARG, "loss, lse or logp is NULL");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (workspace_bytes < flce_forward_workspace_size(T, Hd, V))
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
+                flce_forward_workspace_size(T, Hd, V));
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+
+  if (T == 0) {
+    if (reduction != FLCE_REDUCTION_NONE) CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    if (n_valid) CUDA_TRY(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
+    return FLCE_OK;
+  }
+
+  const int64_t m_blocks = cdiv(T, BM);
+  const int64_t n_blocks = cdiv(V, BN);
+  const int n_split = pick_split(m_blocks, n_blocks, dev->sms);
+  const FwdLayout L = fwd_layout(T, n_split);
+
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = make_map(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
+  if ((st = make_map(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN)) != FLCE_OK) return st;
+  p.num_m_blocks = static_cast<int32_t>(m_blocks);
+  p.num_n_blocks = static_cast<int32_t>(n_blocks);
+  p.num_k_blocks = static_cast<int32_t>(Hd / BK);
+  p.n_split = n_split;
+  p.num_units = static_cast<int32_t>(m_blocks * n_split);
+  p.row0 = 0;
+  p.rows = static_cast<int32_t>(T);
+  p.T = static_cast<int32_t>(T);
+  p.V = static_cast<int32_t>(V);
+  p.part_stride = static_cast<int32_t>(L.part_stride);
+  p.ignore_index = ignore_index;
+  p.targets = targets;
+  p.partials = reinterpret_cast<float2*>(ws + L.partials_off);
+  p.zy = reinterpret_cast<float*>(ws + L.zy_off);
+  p.status = status;
+  p.timeout_ns = g_timeout_ns;
+
+  const double mma_flops = 2.0 * T * Hd * V;
+  const double in_bytes = 2.0 * (T * Hd + V * Hd);
+  {
+    const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
+    KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, mma_flops, in_bytes + 8.0 * n_split * T + 4.0 * T);
+    gemm_kernel<MODE_FWD><<<grid, kThreads, smem_bytes_for(MODE_FWD), s>>>(p);
+    ks.done();
+    if ((st = check_launch("fwd_logits_lse")) != FLCE_OK) return st;
+  }
+  FinalizeParams f;
+  f.partials = p.partials;
+  f.zy = p.zy;
+  f.targets = targets;
+  f.lse = lse;
+  f.logp = logp;
+  f.loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
+  f.block_sum = reinterpret_cast<double*>(ws + L.bsum_off);
+  f.block_count = reinterpret_cast<int64_t*>(ws + L.bcnt_off);
+  f.status = status;
+  f.ignore_index = ignore_index;
+  f.T = static_cast<int32_t>(T);
+  f.V = static_cast<int32_t>(V);
+  f.n_split = n_split;
+  f.part_stride = static_cast<int32_t>(L.part_stride);
+  {
+    KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (8.0 * n_split + 4 + 8 + 12) * T);
+    fwd_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(f);
+    ks.done();
+    if ((st = check_launch("fwd_finalize")) != FLCE_OK) return st;
+  }
+  {
+    KernelScope ks(FLCE_KERNEL_FWD_REDUCE, s, 0.0, 16.0 * L.num_fin_blocks);
+    fwd_reduce_kernel<<<1, kReduceThreads, 0, s>>>(f.block_sum, f.block_count, L.num_fin_blocks, reduction, loss,
+                                                   n_valid);
+    ks.done();
+    if ((st = check_launch("fwd_reduce")) != FLCE_OK) return st;
+  }
+  return FLCE_OK;
+}
+
+flce_status flce_backward(const float* dloss, const void* H, const void* W, const int64_t* targets, const float* lse,
+                          int64_t T, int64_t Hd, int64_t V, int64_t ignore_index, int32_t reduction, void* dH,
+                          float* dW, void* workspace, size_t workspace_bytes, void* stream) {
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
+  if (st != FLCE_OK) return st;
+  if (!dW || (T > 0 && (!dloss || !lse || !dH))) return fail(FLCE_ERR_INVALID_ARG, "dloss, lse, dH or dW is NULL");
+  if ((reinterpret_cast<uintptr_t>(dH) | reinterpret_cast<uintptr_t>(dW)) & 15)
+    return fail(FLCE_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const int64_t chunk = flce_backward_chunk_tokens(T, Hd, V, workspace_bytes);
+  if (chunk <= 0)
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes is too small (need %zu)", workspace_bytes,
+                flce_backward_workspace_size(T, Hd, V));
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+
+  if (T == 0) {
+    CUDA_TRY(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * Hd, s));
+    return FLCE_OK;
+  }
+  const BwdLayout L = bwd_layout(T, V, chunk);
+  float* g = reinterpret_cast<float*>(ws + L.g_off);
+  void* dz = ws + L.dz_off;
+
+  {
+    KernelScope ks(FLCE_KERNEL_BWD_PREP, s, 0.0, 12.0 * T);
+    bwd_prep_kernel<<<1, kReduceThreads, 0, s>>>(dloss, targets, static_cast<int>(T), static_cast<int>(V),
+                                                 ignore_index, reduction, g, status);
+    ks.done();
+    if ((st = check_launch("bwd_prep")) != FLCE_OK) return st;
+  }
+
+  const int64_t n_hd_blocks = cdiv(Hd, BN);
+  CUtensorMap tm_H_k, tm_W_k, tm_W_mn, tm_H_mn, tm_dH, tm_dW_out;
+  if ((st = make_map(&tm_H_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_W_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, 64, 64)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_H_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, 64, 64)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_dH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dH, Hd, T, Hd * 2, 64, 32)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
+
+  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
+    const int64_t rows = std::min<int64_t>(chunk, T - c0);
+    const int64_t m_blocks = cdiv(rows, BM);
+    CUtensorMap tm_dz_store, tm_dz_k, tm_dz_mn;
+    if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 32)) != FLCE_OK)
+      return st;
+    if ((st = make_map(&tm_dz_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, BK, BM)) != FLCE_OK)
+      return st;
+    if ((st = make_map(&tm_dz_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 64)) != FLCE_OK)
+      return st;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.row0 = static_cast<int32_t>(c0);
+    p.rows = static_cast<int32_t>(rows);
+    p.T = static_cast<int32_t>(T);
+    p.V = static_cast<int32_t>(V);
+    p.ignore_index = ignore_index;
+    p.targets = targets;
+    p.lse = lse;
+    p.g = g;
+    p.status = status;
+    p.timeout_ns = g_timeout_ns;
+    p.n_split = 1;
+
+    // (1) recomputed logit tiles -> dZ chunk
+    p.tmA = tm_H_k;
+    p.tmB = tm_W_k;
+    p.tmOut = tm_dz_store;
+    p.num_m_blocks = static_cast<int32_t>(m_blocks);
+    p.num_n_blocks = static_cast<int32_t>(cdiv(V, BN));
+    p.num_k_blocks = static_cast<int32_t>(Hd / BK);
+    p.num_units = p.num_m_blocks * p.num_n_blocks;
+    {
+      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
+      KernelScope ks(FLCE_KERNEL_BWD_DZ, s, 2.0 * rows * Hd * V,
+                     2.0 * (rows * Hd + V * Hd) + 2.0 * rows * V + 16.0 * rows);
+      gemm_kernel<MODE_DZ><<<grid, kThreads, smem_bytes_for(MODE_DZ), s>>>(p);
+      ks.done();
+      if ((st = check_launch("bwd_dz")) != FLCE_OK) return st;
+    }
+    // (2) dH rows of the chunk = dZ W
+    p.tmA = tm_dz_k;
+    p.tmB = tm_W_mn;
+    p.tmOut = tm_dH;
+    p.num_m_blocks = static_cast<int32_t>(m_blocks);
+    p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
+    p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
+    p.num_units = p.num_m_blocks * p.num_n_blocks;
+    {
+      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
+      KernelScope ks(FLCE_KERNEL_BWD_DH, s, 2.0 * rows * Hd * V, 2.0 * rows * V + 2.0 * V * Hd + 2.0 * rows * Hd);
+      gemm_kernel<MODE_DH><<<grid, kThreads, smem_bytes_for(MODE_DH), s>>>(p);
+      ks.done();
+      if ((st = check_launch("bwd_dh")) != FLCE_OK) return st;
+    }
+    // (3) dW (+)= dZ^T H[chunk]; the first chunk stores, later chunks add, in chunk order
+    p.tmA = tm_dz_mn;
+    p.tmB = tm_H_mn;
+    p.tmOut = tm_dW_out;
+    p.num_m_blocks = static_cast<int32_t>(cdiv(V, BM));
+    p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
+    p.num_k_blocks = static_cast<int32_t>(cdiv(rows, BK));
+    p.num_units = p.num_m_blocks * p.num_n_blocks;
+    p.reduce_out = c0 > 0 ? 1 : 0;
+    {
+      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
+      KernelScope ks(FLCE_KERNEL_BWD_DW, s, 2.0 * rows * Hd * V,
+                     2.0 * rows * V + 2.0 * rows * Hd + (c0 > 0 ? 8.0 : 4.0) * V * Hd);
+      gemm_kernel<MODE_DW><<<grid, kThreads, smem_bytes_for(MODE_DW), s>>>(p);
+      ks.done();
+      if ((st = check_launch("bwd_dw")) != FLCE_OK) return st;
+    }
+  }
+  return FLCE_OK;
+}
+
+}  // extern "C"

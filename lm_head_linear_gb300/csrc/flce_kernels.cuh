@@ -1,0 +1,640 @@
+// Kernels of the fused linear cross-entropy for sm_103a.
+//
+// One persistent, warp-specialised tcgen05 GEMM template serves the four
+// contractions of the method (source: "Long-Sequence MoE RL Training: From
+// First Principles to MI300X", section 3):
+//
+//   MODE_FWD  Z = H W^T tile by tile (M = tokens, N = vocab, K = Hd); the
+//             epilogue folds each tile into a per-row running max and sum of
+//             exponentials (the log-sum-exp recurrence) and picks out the
+//             target logit.  Z is never written.
+//   MODE_DZ   the same logit tiles recomputed for one token chunk; the
+//             epilogue forms dZ = g (exp(z - lse) - onehot) in registers and
+//             stores it as bf16 into the [chunk x V] dZ slice.
+//   MODE_DH   dH[chunk] = dZ W        (M = tokens, N = Hd, K = vocab)
+//   MODE_DW   dW (+)= dZ^T H[chunk]   (M = vocab,  N = Hd, K = tokens)
+//
+// CTA layout: 6 warps.  Warp 0: TMA producer (one elected thread).  Warp 1:
+// TMEM allocator and MMA issuer (one elected thread).  Warps 2..5: epilogue;
+// warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows 32*(w%4) .. +31.
+//
+// Tiles are 128 x 256 with 64-deep K blocks: one bf16 K block of a row is
+// 128 bytes, the width of the 128-byte TMA / UMMA swizzle.  Operand tiles pass
+// through a ring of NSTAGE shared-memory stages; the fp32 accumulator lives in
+// TMEM, double-buffered (2 x 256 columns) so that the epilogue of one tile
+// overlaps the MMAs of the next.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace flce {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int NSTAGE = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int STAGING_BOX_BYTES = 32 * 128;     // 32 rows x 128 bytes
+constexpr int STAGING_BYTES = kEpiWarps * 2 * STAGING_BOX_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int kBarriers = 2 * NSTAGE + 5;       // full, empty, tmem_full x2, tmem_empty x2, drain
+constexpr int kSmemTail = 256;                  // barriers + TMEM slot + abort flag
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum Mode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DH = 2, MODE_DW = 3 };
+
+// Device status codes (match flce_status in include/flce.h).
+constexpr int kStatusTargetRange = 6;
+constexpr int kStatusTimeout = 7;
+
+__host__ __device__ constexpr int smem_bytes_for(int mode) {
+  return 1024 + NSTAGE * STAGE_BYTES + (mode == MODE_FWD ? 0 : STAGING_BYTES) + kSmemTail;
+}
+
+struct GemmParams {
+  CUtensorMap tmA;    // operand A (K-major box {64, 128} or MN-major box {64, 64})
+  CUtensorMap tmB;    // operand B (K-major box {64, 256} or MN-major box {64, 64})
+  CUtensorMap tmOut;  // epilogue store / reduce target (unused by MODE_FWD)
+  int32_t num_m_blocks;
+  int32_t num_n_blocks;
+  int32_t num_k_blocks;
+  int32_t n_split;      // MODE_FWD: vocab ranges per token block
+  int32_t num_units;
+  int32_t row0;         // first token of the chunk (0 for MODE_FWD)
+  int32_t rows;         // tokens in the chunk (T for MODE_FWD)
+  int32_t T;
+  int32_t V;
+  int32_t part_stride;  // MODE_FWD: row stride of one split's partials
+  int32_t reduce_out;   // MODE_DW: 0 = store, 1 = reduce-add into the output
+  int32_t pad0;
+  int64_t ignore_index;
+  const int64_t* targets;
+  const float* lse;     // MODE_DZ
+  const float* g;       // MODE_DZ
+  float2* partials;     // MODE_FWD [n_split][part_stride] of (max*log2e, sum of 2^(z*log2e - max))
+  float* zy;            // MODE_FWD [T] target logit
+  int32_t* status;
+  uint64_t timeout_ns;
+};
+
+struct Unit {
+  int m_blk;
+  int n_lo;
+  int n_hi;
+  int split;
+};
+
+template <int MODE>
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+  Unit r;
+  if constexpr (MODE == MODE_FWD) {
+    // split-major order: CTAs running side by side share a vocab range, so
+    // they walk the same W tiles at about the same time and reuse them in L2.
+    const int split = u / p.num_m_blocks;
+    const int base = p.num_n_blocks / p.n_split;
+    const int rem = p.num_n_blocks % p.n_split;
+    r.m_blk = u - split * p.num_m_blocks;
+    r.split = split;
+    r.n_lo = split * base + min(split, rem);
+    r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
+  } else if constexpr (MODE == MODE_DZ) {
+    const int nb = u / p.num_m_blocks;  // token blocks fastest: the W tile is shared in L2
+    r.m_blk = u - nb * p.num_m_blocks;
+    r.n_lo = nb;
+    r.n_hi = nb + 1;
+    r.split = 0;
+  } else {
+    const int mb = u / p.num_n_blocks;  // Hd blocks fastest: the dZ rows are shared in L2
+    r.m_blk = mb;
+    r.n_lo = u - mb * p.num_n_blocks;
+    r.n_hi = r.n_lo + 1;
+    r.split = 0;
+  }
+  return r;
+}
+
+__device__ __forceinline__ void raise_status(int32_t* status, int code) { atomicCAS(status, 0, code); }
+
+struct SmemLayout {
+  uint8_t* stages;
+  uint8_t* staging;
+  uint64_t* bars;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+template <int MODE>
+__device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
+  SmemLayout s;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.stages = base;
+  s.staging = base + NSTAGE * STAGE_BYTES;
+  uint8_t* tail = s.staging + (MODE == MODE_FWD ? 0 : STAGING_BYTES);
+  s.bars = reinterpret_cast<uint64_t*>(tail);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(tail + kBarriers * 8);
+  s.abort_flag = reinterpret_cast<volatile int*>(tail + kBarriers * 8 + 4);
+  return s;
+}
+
+__device__ __forceinline__ uint32_t bar_full(const SmemLayout& s, int i) { return ptx::smem_u32(s.bars + i); }
+__device__ __forceinline__ uint32_t bar_empty(const SmemLayout& s, int i) {
+  return ptx::smem_u32(s.bars + NSTAGE + i);
+}
+__device__ __forceinline__ uint32_t bar_tfull(const SmemLayout& s, int i) {
+  return ptx::smem_u32(s.bars + 2 * NSTAGE + i);
+}
+__device__ __forceinline__ uint32_t bar_tempty(const SmemLayout& s, int i) {
+  return ptx::smem_u32(s.bars + 2 * NSTAGE + 2 + i);
+}
+__device__ __forceinline__ uint32_t bar_drain(const SmemLayout& s) { return ptx::smem_u32(s.bars + 2 * NSTAGE + 4); }
+
+__device__ __forceinline__ void abort_cta(const GemmParams& p, const SmemLayout& s) {
+  *s.abort_flag = 1;
+  raise_status(p.status, kStatusTimeout);
+}
+
+// ----------------------------------------------------------------------------- producer
+template <int MODE>
+__device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLayout& s) {
+  uint32_t stage = 0, phase = 0;
+  uint32_t issued_mask = 0, issued_parity = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    const Unit un = decode_unit<MODE>(p, u);
+    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
+      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        if (!ptx::wait_bounded(bar_empty(s, stage), phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+          abort_cta(p, s);
+          ok = false;
+          break;
+        }
+        const uint32_t full = bar_full(s, stage);
+        ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+        const uint32_t a_dst = ptx::smem_u32(s.stages + stage * STAGE_BYTES);
+        const uint32_t b_dst = a_dst + A_BYTES;
+        const int k0 = kb * BK;
+        if constexpr (MODE == MODE_FWD || MODE == MODE_DZ) {
+          ptx::tma_load_2d(a_dst, &p.tmA, k0, p.row0 + un.m_blk * BM, full);
+          ptx::tma_load_2d(b_dst, &p.tmB, k0, nb * BN, full);
+        } else if constexpr (MODE == MODE_DH) {
+          ptx::tma_load_2d(a_dst, &p.tmA, k0, un.m_blk * BM, full);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) ptx::tma_load_2d(b_dst + j * 8192, &p.tmB, nb * BN + j * 64, k0, full);
+        } else {  // MODE_DW
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            ptx::tma_load_2d(a_dst + j * 8192, &p.tmA, un.m_blk * BM + j * 64, k0, full);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            ptx::tma_load_2d(b_dst + j * 8192, &p.tmB, nb * BN + j * 64, p.row0 + k0, full);
+        }
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == NSTAGE) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+  // Never leave the CTA with TMA writes into its shared memory in flight.
+  for (int i = 0; i < NSTAGE; ++i)
+    if (issued_mask & (1u << i))
+      ptx::wait_bounded(bar_full(s, i), (issued_parity >> i) & 1u, kDrainTimeoutNs, nullptr);
+}
+
+// ----------------------------------------------------------------------------- MMA issuer
+template <int MODE>
+__device__ __forceinline__ void mma_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
+  constexpr uint32_t a_mn = (MODE == MODE_DW) ? 1u : 0u;
+  constexpr uint32_t b_mn = (MODE == MODE_DH || MODE == MODE_DW) ? 1u : 0u;
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, a_mn, b_mn);
+  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    const Unit un = decode_unit<MODE>(p, u);
+    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
+      if (!ptx::wait_bounded(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+        abort_cta(p, s);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        if (!ptx::wait_bounded(bar_full(s, stage), phase, p.timeout_ns, s.abort_flag)) {
+          abort_cta(p, s);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a_addr = ptx::smem_u32(s.stages + stage * STAGE_BYTES);
+        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          // K-major: the 16-deep slice is 32 bytes further along the swizzled
+          // 128-byte row; 8-row groups are 1024 bytes apart.  MN-major: the
+          // slice is 16 rows (2048 bytes) further; 64-wide MN blocks are 8 KB apart.
+          const uint64_t a_desc = a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                       : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t b_desc = b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                       : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar_empty(s, stage));
+        if (++stage == NSTAGE) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      ptx::mma_commit(bar_tfull(s, acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  // Wait for every MMA issued so far before TMEM is freed.
+  ptx::mma_commit(bar_drain(s));
+  ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
+}
+
+// ----------------------------------------------------------------------------- epilogues
+// TMEM load of 32 columns for this warp's 32 rows, completed before return.
+__device__ __forceinline__ void tmem_load32_sync(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  ptx::tmem_ld32(taddr, r);
+  ptx::tmem_wait_ld32(r);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Write eight 16-byte chunks (32 words) of this lane's staging row using the
+// 128-byte swizzle the TMA store expects: chunk k of row r lands at
+// r*128 + ((k ^ (r % 8)) * 16).
+__device__ __forceinline__ void stage_row_words(uint32_t buf, int lane, const uint32_t (&w)[32]) {
+  const uint32_t row = buf + lane * 128;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    ptx::st_shared_v4(row + ((k ^ (lane & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base,
+                                              int warp, int lane) {
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const int row_in_tile = q * 32 + lane;
+  const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  uint32_t acc = 0, acc_phase = 0;
+  uint32_t box_count = 0;  // staging buffers alternate per stored box
+  const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
+  bool ok = true;
+
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    const Unit un = decode_unit<MODE>(p, u);
+    const int t_local = un.m_blk * BM + row_in_tile;  // M index within the launch
+
+    float m_run = -INFINITY, s_run = 0.0f, zy = 0.0f;
+    bool have_zy = false;
+    int y = -1;
+    float gt = 0.0f, lse2 = 0.0f;
+    if constexpr (MODE == MODE_FWD) {
+      if (t_local < p.rows) {
+        const int64_t yy = p.targets[t_local];
+        if (yy != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
+      }
+    } else if constexpr (MODE == MODE_DZ) {
+      if (t_local < p.rows) {
+        const int t = p.row0 + t_local;
+        gt = p.g[t];
+        lse2 = p.lse[t] * kLog2e;
+        const int64_t yy = p.targets[t];
+        if (yy >= 0 && yy < p.V) y = static_cast<int>(yy);
+      }
+    }
+
+    for (int nb = un.n_lo; nb < un.n_hi; ++nb) {
+      if (!ptx::wait_bounded(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
+        abort_cta(p, s);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t tcol = lane_addr + acc * BN;
+
+      if constexpr (MODE == MODE_FWD) {
+        const int n0 = nb * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_load32_sync(tcol + c * 32, v);
+          const int col0 = n0 + c * 32;
+          if (col0 + 32 > p.V) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j >= p.V) v[j] = -INFINITY;
+          }
+          const int yo = y - col0;
+          if (static_cast<unsigned>(yo) < 32u) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == yo) zy = v[j];
+            have_zy = true;
+          }
+          float mx = v[0];
+#pragma unroll
+          for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
+          const float m_new = fmaxf(m_run, mx * kLog2e);
+          float acc_s = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc_s += ptx::ex2(fmaf(v[j], kLog2e, -m_new));
+          s_run = s_run * ptx::ex2(m_run - m_new) + acc_s;
+          m_run = m_new;
+        }
+      } else if constexpr (MODE == MODE_DZ || MODE == MODE_DH) {
+#pragma unroll 1
+        for (int j = 0; j < BN / 64; ++j) {
+          uint32_t w[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_load32_sync(tcol + j * 64 + h * 32, v);
+            if constexpr (MODE == MODE_DZ) {
+              const int col0 = nb * BN + j * 64 + h * 32;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = ptx::ex2(fmaf(v[i], kLog2e, -lse2));
+              const int yo = y - col0;
+              if (static_cast<unsigned>(yo) < 32u) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i == yo) v[i] -= 1.0f;
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= gt;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[h * 16 + i] = ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          }
+          const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
+          if (lane == 0) ptx::bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_words(buf, lane, w);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x = nb * BN + j * 64;
+            const int yrow = (MODE == MODE_DZ ? 0 : p.row0) + un.m_blk * BM + q * 32;
+            ptx::tma_store_2d(&p.tmOut, buf, x, yrow);
+            ptx::bulk_commit();
+          }
+          ++box_count;
+        }
+      } else {  // MODE_DW: fp32 boxes of 32 columns
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+          float v[32];
+          tmem_load32_sync(tcol + j * 32, v);
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+          const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
+          if (lane == 0) ptx::bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_words(buf, lane, w);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x = nb * BN + j * 32;
+            const int yrow = un.m_blk * BM + q * 32;
+            if (p.reduce_out)
+              ptx::tma_reduce_add_2d(&p.tmOut, buf, x, yrow);
+            else
+              ptx::tma_store_2d(&p.tmOut, buf, x, yrow);
+            ptx::bulk_commit();
+          }
+          ++box_count;
+        }
+      }
+
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_tempty(s, acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+
+    if constexpr (MODE == MODE_FWD) {
+      if (ok && t_local < p.rows) {
+        p.partials[static_cast<size_t>(un.split) * p.part_stride + t_local] = make_float2(m_run, s_run);
+        if (have_zy) p.zy[t_local] = zy;
+      }
+    }
+  }
+  if (lane == 0) ptx::bulk_wait<0>();
+  __syncwarp();
+}
+
+// ----------------------------------------------------------------------------- the GEMM kernel
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const SmemLayout s = carve_smem<MODE>(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      ptx::mbar_init(bar_full(s, i), 1);
+      ptx::mbar_init(bar_empty(s, i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar_tfull(s, i), 1);
+      ptx::mbar_init(bar_tempty(s, i), kEpiWarps);
+    }
+    ptx::mbar_init(bar_drain(s), 1);
+    *s.abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&p.tmA);
+    ptx::prefetch_tmap(&p.tmB);
+    if (MODE != MODE_FWD) ptx::prefetch_tmap(&p.tmOut);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *s.tmem_slot;
+
+  if (warp == 0) {
+    if (ptx::elect_one()) producer_loop<MODE>(p, s);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (ptx::elect_one()) mma_loop<MODE>(p, s, tmem_base);
+    __syncwarp();
+  } else {
+    epilogue_loop<MODE>(p, s, tmem_base, warp, lane);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ----------------------------------------------------------------------------- forward finalize
+// Per row: merge the vocab-range partials in split order into lse, then
+// loss_t = lse - z_y and logp_t = z_y - lse on valid rows.  Each block also
+// writes the fixed-order sum of its rows' losses and its count of valid rows.
+constexpr int kFinalizeThreads = 256;
+
+struct FinalizeParams {
+  const float2* partials;
+  const float* zy;
+  const int64_t* targets;
+  float* lse;
+  float* logp;
+  float* loss_rows;      // [T] when reduction is NONE, else nullptr
+  double* block_sum;     // [num_blocks]
+  int64_t* block_count;  // [num_blocks]
+  int32_t* status;
+  int64_t ignore_index;
+  int32_t T;
+  int32_t V;
+  int32_t n_split;
+  int32_t part_stride;
+};
+
+__global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(const FinalizeParams p) {
+  __shared__ double sh_sum[kFinalizeThreads];
+  __shared__ long long sh_cnt[kFinalizeThreads];
+  const int t = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  double my_loss = 0.0;
+  long long my_cnt = 0;
+  if (t < p.T) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < p.n_split; ++sp) M = fmaxf(M, p.partials[static_cast<size_t>(sp) * p.part_stride + t].x);
+    float S = 0.0f;
+    for (int sp = 0; sp < p.n_split; ++sp) {
+      const float2 pr = p.partials[static_cast<size_t>(sp) * p.part_stride + t];
+      S += pr.y * exp2f(pr.x - M);
+    }
+    const float lse = (M + log2f(S)) * kLn2;
+    const int64_t y = p.targets[t];
+    bool valid = y != p.ignore_index;
+    if (valid && (y < 0 || y >= p.V)) {
+      raise_status(p.status, kStatusTargetRange);
+      valid = false;
+    }
+    float loss_t = 0.0f, logp_t = 0.0f;
+    if (valid) {
+      const float z = p.zy[t];
+      loss_t = lse - z;
+      logp_t = z - lse;
+      my_loss = static_cast<double>(loss_t);
+      my_cnt = 1;
+    }
+    p.lse[t] = lse;
+    p.logp[t] = logp_t;
+    if (p.loss_rows) p.loss_rows[t] = loss_t;
+  }
+  sh_sum[threadIdx.x] = my_loss;
+  sh_cnt[threadIdx.x] = my_cnt;
+  __syncthreads();
+  for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      sh_sum[threadIdx.x] += sh_sum[threadIdx.x + w];
+      sh_cnt[threadIdx.x] += sh_cnt[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.block_sum[blockIdx.x] = sh_sum[0];
+    p.block_count[blockIdx.x] = sh_cnt[0];
+  }
+}
+
+// One block: fixed-order sum of the block partials into the scalar loss and n_valid.
+constexpr int kReduceThreads = 1024;
+
+__global__ void __launch_bounds__(kReduceThreads) fwd_reduce_kernel(const double* block_sum, const int64_t* block_count,
+                                                                    int num_blocks, int reduction, float* loss,
+                                                                    int64_t* n_valid) {
+  __shared__ double sh_sum[kReduceThreads];
+  __shared__ long long sh_cnt[kReduceThreads];
+  double a = 0.0;
+  long long c = 0;
+  for (int i = threadIdx.x; i < num_blocks; i += kReduceThreads) {
+    a += block_sum[i];
+    c += block_count[i];
+  }
+  sh_sum[threadIdx.x] = a;
+  sh_cnt[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = kReduceThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      sh_sum[threadIdx.x] += sh_sum[threadIdx.x + w];
+      sh_cnt[threadIdx.x] += sh_cnt[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double total = sh_sum[0];
+    const long long n = sh_cnt[0];
+    if (reduction == 1) loss[0] = n > 0 ? static_cast<float>(total / static_cast<double>(n)) : 0.0f;
+    if (reduction == 2) loss[0] = static_cast<float>(total);
+    if (n_valid) n_valid[0] = n;
+  }
+}
+
+// ----------------------------------------------------------------------------- backward prep
+// One block: count valid rows (fixed-order tree), flag out-of-range targets,
+// then write the per-token upstream weight g_t.
+__global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* dloss, const int64_t* targets, int T,
+                                                                  int V, int64_t ignore_index, int reduction,
+                                                                  float* g, int32_t* status) {
+  __shared__ long long sh_cnt[kReduceThreads];
+  long long c = 0;
+  bool bad = false;
+  for (int t = threadIdx.x; t < T; t += kReduceThreads) {
+    const int64_t y = targets[t];
+    if (y != ignore_index) {
+      if (y >= 0 && y < V)
+        ++c;
+      else
+        bad = true;
+    }
+  }
+  if (bad) raise_status(status, kStatusTargetRange);
+  sh_cnt[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = kReduceThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) sh_cnt[threadIdx.x] += sh_cnt[threadIdx.x + w];
+    __syncthreads();
+  }
+  const long long n = sh_cnt[0];
+  const float scalar = (reduction == 1) ? (n > 0 ? dloss[0] / static_cast<float>(n) : 0.0f)
+                                        : (reduction == 2 ? dloss[0] : 0.0f);
+  for (int t = threadIdx.x; t < T; t += kReduceThreads) {
+    const int64_t y = targets[t];
+    const bool valid = (y != ignore_index) && y >= 0 && y < V;
+    g[t] = valid ? (reduction == 0 ? dloss[t] : scalar) : 0.0f;
+  }
+}
+
+}  // namespace flce

@@ -1,0 +1,90 @@
+"""The C-ABI library builds, loads, and exports every symbol include/flce.h declares.
+
+No compute call is made here (no GPU needed); host-only entry points
+(workspace sizing, status strings, ABI version, argument checks) are exercised.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import lm_head_linear_gb300 as flce
+from lm_head_linear_gb300 import build as flce_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+
+def declared_symbols():
+    src = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"FLCE_API\s+[\w\s\*]+?\b(flce_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    flce_build.build()
+    return flce.load_library()
+
+
+def test_header_declares_the_two_calls():
+    syms = declared_symbols()
+    assert "flce_forward" in syms and "flce_backward" in syms
+    assert len(syms) >= 13
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in flce.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_exported_symbols_are_only_the_declared_ones(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", flce_build.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted({ln.split()[-1] for ln in out.splitlines()
+                       if " T " in ln and ln.split()[-1].startswith("flce_")})
+    assert exported == declared_symbols()
+
+
+def test_host_only_entry_points(lib):
+    assert lib.flce_abi_version() == 1
+    assert lib.flce_status_string(0) == b"FLCE_OK"
+    assert lib.flce_status_string(6) == b"FLCE_ERR_TARGET_RANGE"
+    assert lib.flce_kernel_name(4) == b"bwd_dz"
+    T, Hd, V = 65536, 2048, 124160
+    fws = lib.flce_forward_workspace_size(T, Hd, V)
+    bws = lib.flce_backward_workspace_size(T, Hd, V)
+    assert 0 < fws < 64 * 2**20
+    # the backward keeps a [chunk x V] bf16 slice of dZ, never [T x V]
+    assert bws < T * V * 2
+    chunk = lib.flce_backward_chunk_tokens(T, Hd, V, bws)
+    assert 128 <= chunk < T and chunk % 128 == 0
+    assert bws >= chunk * V * 2
+    assert lib.flce_backward_chunk_tokens(T, Hd, V, 1024) == 0
+    # a bigger workspace gives a bigger chunk, capped at T rounded up to 128
+    assert lib.flce_backward_chunk_tokens(T, Hd, V, bws * 4) > chunk
+    assert lib.flce_backward_chunk_tokens(1000, 64, 50, 2**30) == 1024
+    for t in (257, 1000, 8192, 131072):
+        assert lib.flce_backward_workspace_size(t, 4096, 124160) < t * 124160 * 2
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    # Host-side validation needs no device: bad sizes and NULLs are rejected first.
+    P = ctypes.c_void_p
+    st = lib.flce_forward(P(16), P(16), P(16), 10, 100, 50, -100, 1, P(16), P(16), P(16), None, P(256), 1 << 20, None)
+    assert st == 2  # Hd not a multiple of 64
+    st = lib.flce_forward(P(16), P(16), P(16), 10, 64, 50, 3, 1, P(16), P(16), P(16), None, P(256), 1 << 20, None)
+    assert st == 1  # ignore_index inside [0, V)
+    st = lib.flce_forward(P(16), P(16), P(16), 10, 64, 50, -100, 7, P(16), P(16), P(16), None, P(256), 1 << 20, None)
+    assert st == 1  # unknown reduction
+    st = lib.flce_forward(P(16), P(18), P(16), 10, 64, 50, -100, 1, P(16), P(16), P(16), None, P(256), 1 << 20, None)
+    assert st == 3  # misaligned W
+    st = lib.flce_forward(P(16), P(16), P(16), 10, 64, 50, -100, 1, P(16), P(16), P(16), None, P(256), 16, None)
+    assert st == 4  # workspace too small
+    st = lib.flce_backward(P(16), P(16), P(16), P(16), P(16), 10, 64, 50, -100, 1, P(16), P(16), P(256), 16, None)
+    assert st == 4
+    st = lib.flce_forward(None, P(16), P(16), 10, 64, 50, -100, 1, P(16), P(16), P(16), None, P(256), 1 << 20, None)
+    assert st == 1
+    assert b"NULL" in lib.flce_last_error()

@@ -1,0 +1,217 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Element-by-element on shapes the oracle finishes in seconds that span several
+128 x 256 tiles and ragged tails; sampled rows and size-independent properties
+on the five full-size workloads.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import lm_head_linear_gb300 as flce
+import oracle
+from workloads import generate, workload
+
+from gpu_helpers import TOL_GRAD, TOL_TOKEN, check_token_outputs, rel_fro, run, to_device
+
+pytestmark = pytest.mark.gpu
+
+# name -> (workload recipe, T, Hd, V): every case spans several tiles and has ragged edges.
+FULL_CASES = {
+    "tiny_T256_H256_V4096": ("tiny", None, None, None),
+    "zipf_mean_T1000_H256_V5000": ("medium", 1000, 256, 5000),
+    "uniform_sum_T333_H320_V777": ("long", 333, 320, 777),
+    "rl_none_T768_H192_V3001": ("rlpg", 768, 192, 3001),
+    "outliers_T640_H512_V4097": ("lmhead", 640, 512, 4097),
+}
+
+
+def _full_check(inp, out):
+    H64, W64 = inp.H64(), inp.W64()
+    ref = oracle.forward(H64, W64, inp.targets, inp.ignore_index, inp.reduction)
+    valid = inp.targets != inp.ignore_index
+    assert out["fwd_status"] == 0 and out["bwd_status"] == 0
+    assert int(out["n_valid"].item()) == ref.n_valid
+    check_token_outputs(out, {"lse": ref.lse, "logp": ref.logp, "loss_tok": ref.loss_tok}, valid, inp.reduction)
+    if inp.reduction != "none":
+        assert abs(float(out["loss"].item()) - float(ref.loss)) <= TOL_TOKEN
+    dH_ref, dW_ref = oracle.backward(inp.dloss, H64, W64, inp.targets, inp.ignore_index, inp.reduction)
+    dH = out["dH"].float().cpu().numpy()
+    dW = out["dW"].cpu().numpy()
+    assert rel_fro(dH, dH_ref) <= TOL_GRAD, rel_fro(dH, dH_ref)
+    assert rel_fro(dW, dW_ref) <= TOL_GRAD, rel_fro(dW, dW_ref)
+    assert np.all(dH[~valid] == 0.0)
+
+
+@pytest.mark.parametrize("case", sorted(FULL_CASES))
+def test_full_oracle(case, cuda_device):
+    wl, T, Hd, V = FULL_CASES[case]
+    inp = generate(wl, T=T, Hd=Hd, V=V, n_seq=8 if wl == "rlpg" else None)
+    _full_check(inp, run(inp, cuda_device))
+
+
+def test_many_token_chunks(cuda_device):
+    """A workspace sized for 128-token chunks: dW accumulates over 8 chunks in order."""
+    inp = generate("medium", T=1000, Hd=256, V=5000)
+    ws = flce.flce_backward_workspace_size(1000, 256, 5000)
+    chunk_ws = 5120 + 2 * 128 * 5056
+    assert flce.flce_backward_chunk_tokens(1000, 256, 5000, chunk_ws) == 128
+    assert chunk_ws < ws
+    _full_check(inp, run(inp, cuda_device, bwd_workspace_bytes=chunk_ws))
+
+
+def test_deterministic(cuda_device):
+    inp = generate("medium", T=1000, Hd=256, V=5000)
+    a = run(inp, cuda_device)
+    b = run(inp, cuda_device)
+    for k in ("loss", "lse", "logp", "dH", "dW"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_running_max_is_load_bearing(cuda_device):
+    """Every logit carries +200 (hidden column 0 = 8, weight column 0 = 25, both exact in
+    bf16): exp(z) overflows fp32, the running-max recurrence must not."""
+    inp = generate("tiny", T=300, Hd=128, V=1000)
+    H = inp.H_bits.copy()
+    W = inp.W_bits.copy()
+    H[:, 0] = 0x4100  # 8.0
+    W[:, 0] = 0x41C8  # 25.0
+    inp.H_bits, inp.W_bits = H, W
+    out = run(inp, cuda_device)
+    assert np.all(np.isfinite(out["lse"].cpu().numpy()))
+    assert out["lse"].cpu().numpy().min() > 150.0
+    _full_check(inp, out)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_vocab_of_one(cuda_device):
+    inp = generate("tiny", T=130, Hd=64, V=1)
+    out = run(inp, cuda_device)
+    _full_check(inp, out)
+    assert np.abs(out["loss"].cpu().numpy()).max() <= TOL_TOKEN
+
+
+def test_all_rows_ignored(cuda_device):
+    inp = generate("tiny", T=200, Hd=64, V=300)
+    inp.targets[:] = inp.ignore_index
+    out = run(inp, cuda_device)
+    assert int(out["n_valid"].item()) == 0
+    assert float(out["loss"].item()) == 0.0
+    assert not out["dH"].float().abs().sum().item() and not out["dW"].abs().sum().item()
+
+
+def test_single_token_and_empty(cuda_device):
+    inp = generate("tiny", T=1, Hd=64, V=700)
+    _full_check(inp, run(inp, cuda_device))
+    e = generate("tiny", T=0, Hd=64, V=700)
+    out = run(e, cuda_device)
+    assert float(out["loss"].item()) == 0.0 and int(out["n_valid"].item()) == 0
+    assert out["dH"].numel() == 0 and not out["dW"].abs().sum().item()
+
+
+def test_target_out_of_range_sets_device_status(cuda_device):
+    inp = generate("tiny", T=200, Hd=64, V=300)
+    inp.targets[5] = 300
+    out = run(inp, cuda_device)
+    assert out["fwd_status"] == 6 and out["bwd_status"] == 6
+    # the bad row is treated as ignored; everything else is still right
+    inp.targets[5] = inp.ignore_index
+    ok = run(inp, cuda_device)
+    assert torch.equal(out["loss"], ok["loss"]) and torch.equal(out["dW"], ok["dW"])
+
+
+def test_argument_errors(cuda_device):
+    inp = generate("tiny", T=64, Hd=64, V=100)
+    H, W, y, _ = to_device(inp, cuda_device)
+    with pytest.raises(flce.FlceError) as e:
+        flce.flce_forward(H, W, y, ignore_index=5)
+    assert e.value.status == 1
+    with pytest.raises(flce.FlceError) as e:
+        flce.flce_forward(H, W, y, workspace=torch.empty(64, dtype=torch.uint8, device=cuda_device))
+    assert e.value.status == 4
+
+
+def test_autograd_wrapper(cuda_device):
+    inp = generate("medium", T=300, Hd=128, V=2000)
+    H, W, y, _ = to_device(inp, cuda_device)
+    Hr = H.clone().requires_grad_(True)
+    Wr = W.clone().requires_grad_(True)
+    loss = flce.linear_cross_entropy(Hr, Wr, y)
+    loss.backward()
+    dH_ref, dW_ref = oracle.backward(1.0, inp.H64(), inp.W64(), inp.targets, -100, "mean")
+    assert rel_fro(Hr.grad.float().cpu().numpy(), dH_ref) <= TOL_GRAD
+    assert rel_fro(Wr.grad.float().cpu().numpy(), dW_ref) <= TOL_GRAD
+
+
+# ------------------------------------------------------------------ the five full-size workloads
+
+FULL_SIZE = ["tiny", "medium", "lmhead", "long", "rlpg"]
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_workload(name, cuda_device):
+    """Full-size run in the bench's launch configuration: sampled token rows against the
+    oracle (lse, logp, loss, dH), and for dW the properties that hold at any size:
+    sum_v dW_v = 0 up to the bf16 rounding of dZ, and <dW, W> = <dH, H>."""
+    wl = workload(name)
+    inp = generate(wl)
+    torch.cuda.reset_peak_memory_stats(cuda_device)
+    base = torch.cuda.memory_allocated(cuda_device)
+    out = run(inp, cuda_device)
+    peak_extra = torch.cuda.max_memory_allocated(cuda_device) - base
+    assert out["fwd_status"] == 0 and out["bwd_status"] == 0
+    T, V, Hd = inp.T, inp.V, inp.Hd
+    # never a [T x V] buffer: the workspace stays below one bf16 logits copy, and so does
+    # everything allocated beyond the inputs and the dH / dW outputs
+    if T > 256:
+        assert flce.flce_backward_workspace_size(T, Hd, V) < T * V * 2
+        assert peak_extra < T * V * 2 + 4 * V * Hd + 4 * T * Hd + 2 * V * Hd
+    valid = inp.targets != inp.ignore_index
+    assert int(out["n_valid"].item()) == int(valid.sum())
+    rng = np.random.default_rng(123)
+    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=min(T, 40), replace=False),
+                                     np.nonzero(~valid)[0][:4]]))
+    W64 = inp.W64()
+    g = oracle.upstream_grad(inp.dloss, inp.targets, V, inp.ignore_index, inp.reduction)
+    ref = oracle.sampled_rows(inp.H64(rows), W64, inp.targets[rows], g[rows], inp.ignore_index)
+    del W64
+    check_token_outputs(out, ref, valid[rows], inp.reduction, rows=rows)
+    dH = out["dH"].float()
+    dH_rows = dH[torch.from_numpy(rows).to(cuda_device)].cpu().numpy()
+    assert rel_fro(dH_rows, ref["dH"]) <= TOL_GRAD, rel_fro(dH_rows, ref["dH"])
+    assert np.all(dH_rows[~valid[rows]] == 0.0)
+
+    dW = out["dW"]
+    H_dev, W_dev = to_device(inp, cuda_device)[:2]
+    # (1) sum_v dW_v = sum_t (sum_v dZ_tv) h_t; each stored dZ element carries a relative
+    #     rounding error <= 2^-9 and sum_v |dZ_tv| <= 2|g_t|, so |sum_v dW_v| <= 2^-8 sum_t |g_t| |h_t|.
+    colsum = dW.double().sum(dim=0).cpu().numpy()
+    hnorm = H_dev.float().norm(dim=1).double().cpu().numpy()
+    bound = 2.0 ** -8 * float(np.sum(np.abs(g) * hnorm)) + 1e-6
+    assert np.linalg.norm(colsum) <= bound, (np.linalg.norm(colsum), bound)
+    # (2) <dW, W> = sum_t sum_v dZ_tv z_tv = <dH, H>
+    lhs = float((dW.double() * W_dev.double()).sum().item())
+    rhs = float((dH.double() * H_dev.double()).sum().item())
+    assert abs(lhs - rhs) <= TOL_GRAD * max(abs(lhs), abs(rhs)) + 1e-6, (lhs, rhs)
+    assert float(dW.abs().max().item()) > 0.0
+
+
+def test_full_size_sampled_dW_medium(cuda_device):
+    """Sampled vocab rows of dW at the full medium size (T=8192, Hd=2048, V=124,160) against
+    the oracle; needs the oracle's lse on every token (one fp64 pass over T x V)."""
+    inp = generate("medium")
+    out = run(inp, cuda_device)
+    H64, W64 = inp.H64(), inp.W64()
+    ref = oracle.forward(H64, W64, inp.targets, inp.ignore_index, inp.reduction, row_block=512)
+    g = oracle.upstream_grad(inp.dloss, inp.targets, inp.V, inp.ignore_index, inp.reduction)
+    rng = np.random.default_rng(7)
+    vr = np.unique(np.concatenate([[0, 1, inp.V - 1], rng.choice(inp.V, 29, replace=False),
+                                   inp.targets[inp.targets >= 0][:4]]))
+    dW_ref = oracle.dW_rows(H64, W64[vr], inp.targets, g, ref.lse, vr)
+    dW_rows = out["dW"][torch.from_numpy(vr).to(cuda_device)].cpu().numpy()
+    assert rel_fro(dW_rows, dW_ref) <= TOL_GRAD, rel_fro(dW_rows, dW_ref)
+    lse = out["lse"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse - ref.lse)) <= TOL_TOKEN
+    assert abs(float(out["loss"].item()) - float(ref.loss)) <= TOL_TOKEN
