@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Benchmark: fused linear cross-entropy forward + backward on GB300.
+
+One step = flce_forward + flce_backward over one batch of the workload (all
+steps of the path: logit tiles with the log-sum-exp epilogue, finalize, dZ
+recompute, dH and dW contractions).  The default workload is 65,536 tokens x
+hidden 2048 x vocab 124,160 (bf16 inputs, fp32 accumulation).
+
+Prints one JSON line.  ``value`` is whole-job tokens/s with the inputs resident
+in HBM; ``e2e`` is the same metric through the public API with the inputs in
+pinned host memory, copied in and the loss and gradients copied back inside the
+timed region.  ``--impl reference`` times the fp64 CPU oracle on the host cores
+instead (a bounded sample of the same workload).
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the op
+shards by token batches with no exchange inside it), the timed region is
+bracketed by barriers, and the max over ranks is reported.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import generate, workload  # noqa: E402
+
+METRIC = "fused linear-CE fwd+bwd tokens/s (T=64K,V=124,160); % of GB300 BF16 TC peak"
+DEFAULT_WORKLOAD = "lmhead_T65536_H2048_V124160"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("csrc/flce_kernels.cuh", "csrc/ptx.cuh", "csrc/flce_api.cu"):
+        with open(os.path.join(ROOT, "lm_head_linear_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        data = json.load(fh)
+    rec = data.get(kernel)
+    if not rec or rec.get("source_sha") != kernel_source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def time_oracle(inp, budget_s=12.0, slice_tokens=128, W64=None):
+    """Tokens/s of the fp64 oracle (as it stands) on slices of the workload's tokens:
+    forward + backward for each slice with the full vocabulary."""
+    import oracle
+    if W64 is None:
+        W64 = inp.W64()
+    t_start = time.perf_counter()
+    done = 0
+    s0 = 0
+    while True:
+        rows = np.arange(s0, min(s0 + slice_tokens, inp.T))
+        H64 = inp.H64(rows)
+        y = inp.targets[rows]
+        dl = inp.dloss[rows] if inp.reduction == "none" else inp.dloss
+        oracle.forward(H64, W64, y, inp.ignore_index, inp.reduction)
+        oracle.backward(dl, H64, W64, y, inp.ignore_index, inp.reduction)
+        done += len(rows)
+        s0 = (s0 + slice_tokens) % inp.T
+        el = time.perf_counter() - t_start
+        if el >= budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": done / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} tokens in {slice_tokens}-token slices, forward + backward over the full "
+                      f"V={inp.V}, Hd={inp.Hd}, fp64 numpy, {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    wl = workload(args.workload)
+    inp = generate(wl)
+    W64 = inp.W64()
+    for _ in range(args.warmup):
+        time_oracle(inp, budget_s=0.0, slice_tokens=32, W64=W64)
+    per = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        per.append(time_oracle(inp, budget_s=args.ref_step_seconds, slice_tokens=64, W64=W64))
+    el = time.perf_counter() - t0
+    value = sum(r["value"] for r in per) / len(per)
+    tokens = value * el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.T / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "Hd": wl.Hd, "V": wl.V,
+                                        "reduction": wl.reduction},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": per[0]["cores"], "kind": "oracle",
+                         "sample": f"each step: {per[0]['sample']}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "tokens_timed": int(tokens),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import lm_head_linear_gb300 as flce
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    wl = workload(args.workload)
+    inp = generate(wl, seed=rank)
+    T, Hd, V = inp.T, inp.Hd, inp.V
+    stream = torch.cuda.current_stream(dev)
+
+    H_h = torch.from_numpy(inp.H_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_h = torch.from_numpy(inp.W_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_h = torch.from_numpy(inp.targets).pin_memory()
+    dl_h = torch.from_numpy(inp.dloss).pin_memory()
+    H = H_h.to(dev)
+    W = W_h.to(dev)
+    y = y_h.to(dev)
+    dloss = dl_h.to(dev)
+    out_f = {"loss": torch.empty(T if wl.reduction == "none" else 1, dtype=torch.float32, device=dev),
+             "lse": torch.empty(T, dtype=torch.float32, device=dev),
+             "logp": torch.empty(T, dtype=torch.float32, device=dev),
+             "n_valid": torch.empty(1, dtype=torch.int64, device=dev)}
+    out_b = {"dH": torch.empty((T, Hd), dtype=torch.bfloat16, device=dev),
+             "dW": torch.empty((V, Hd), dtype=torch.float32, device=dev)}
+    fws = torch.empty(flce.flce_forward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
+    bws = torch.empty(flce.flce_backward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
+
+    def step(Hx, Wx, yx, dlx):
+        flce.flce_forward(Hx, Wx, yx, inp.ignore_index, wl.reduction, workspace=fws, out=out_f)
+        flce.flce_backward(dlx, Hx, Wx, yx, out_f["lse"], inp.ignore_index, wl.reduction, workspace=bws, out=out_b)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step(H, W, y, dloss)
+    barrier()
+    for k in ("fwd", "bwd"):
+        st = flce.flce_read_device_status(fws if k == "fwd" else bws)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the warm-up {k}")
+
+    # ---- device-resident timed region (value); per-kernel events for the roofline
+    flce.flce_profile_collect()
+    flce.flce_profile_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(H, W, y, dloss)
+        ev1.record(stream)
+        barrier()
+    flce.flce_profile_enable(False)
+    kstats = flce.flce_profile_collect()
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1))
+    ms_step = ms_total / args.steps
+    value = world * T * args.steps / (ms_total / 1000.0)
+    gpu_launches = sum(v["launches"] for v in kstats.values())
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = max(1, min(args.steps, 5))
+    dH_h = torch.empty((T, Hd), dtype=torch.bfloat16).pin_memory()
+    dW_h = torch.empty((V, Hd), dtype=torch.float32).pin_memory()
+    loss_h = torch.empty_like(out_f["loss"], device="cpu").pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        H.copy_(H_h, non_blocking=True)
+        W.copy_(W_h, non_blocking=True)
+        y.copy_(y_h, non_blocking=True)
+        dloss.copy_(dl_h, non_blocking=True)
+        step(H, W, y, dloss)
+        loss_h.copy_(out_f["loss"], non_blocking=True)
+        dH_h.copy_(out_b["dH"], non_blocking=True)
+        dW_h.copy_(out_b["dW"], non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    h2d = H_h.numel() * 2 + W_h.numel() * 2 + y_h.numel() * 8 + dl_h.numel() * 4
+    d2h = loss_h.numel() * 4 + dH_h.numel() * 2 + dW_h.numel() * 4
+    e2e = {"value": world * T * e2e_steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    flops_step = 8.0 * T * Hd * V
+    tflops = world * flops_step * args.steps / (ms_total / 1000.0) / 1e12
+    dom_name, dom = max(kstats.items(), key=lambda kv: kv[1]["total_ms"])
+    avg_ms = dom["total_ms"] / dom["launches"]
+    ach = (dom["flops"] / dom["launches"]) / (avg_ms / 1000.0) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = traffic_from_profiles(dom_name)
+    kernels = {k: {"launches": v["launches"], "avg_ms": v["total_ms"] / v["launches"],
+                   "share": v["total_ms"] / sum(x["total_ms"] for x in kstats.values()),
+                   "tflops": (v["flops"] / (v["total_ms"] / 1000.0) / 1e12) if v["flops"] else None}
+               for k, v in sorted(kstats.items())}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "Hd": Hd, "V": V, "reduction": wl.reduction,
+                   "backward_chunk_tokens": flce.flce_backward_chunk_tokens(T, Hd, V, bws.numel()),
+                   "l2": "inputs larger than L2 (H %.0f MB + W %.0f MB > 129 MB), no flush" % (
+                       T * Hd * 2 / 1e6, V * Hd * 2 / 1e6),
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "tflops": tflops,
+        "frac_of_bf16_peak": {"burst": tflops / float(peaks.get("bf16_tflops", 1)),
+                              "sustained": tflops / peak, "source": peak_src},
+        "model_tflops_6THV": tflops * 6.0 / 8.0,
+        "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                     "frac": ach / peak, "traffic": traffic,
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                     "algorithmic_flops_per_launch": dom["flops"] / dom["launches"]},
+        "kernels": kernels,
+        "gpu_launches": int(gpu_launches),
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+        "peak_extra_bytes": int(fws.numel() + bws.numel()),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(inp, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
