@@ -126,6 +126,32 @@ FLCE_API flce_status flce_backward(const float* dloss, const void* H, const void
                                    int32_t reduction, void* dH, float* dW, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Forward without any allocation by the caller or the library.  The pages
+ * have no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory at the point where they need the loss: code whose
+ * framework allocator owns all of device memory, plugin hooks of inference or
+ * training engines that are not allowed to allocate, and latency-critical
+ * paths that forbid allocation.  Such callers pass only inputs and outputs.
+ *
+ * Arguments and results are those of flce_forward(); instead of a workspace,
+ * the call uses a scratch array built into the library: a 32 MiB device array
+ * that every GPU which loads the library holds until the process exits.  That
+ * limits T to at most 253,952 tokens (any Hd and V); larger T is rejected with
+ * FLCE_ERR_WORKSPACE before anything is launched.  The device status word of
+ * the call (0, FLCE_ERR_TARGET_RANGE or FLCE_ERR_TIMEOUT) is copied into
+ * *device_status (a device int32) unless it is NULL.
+ *
+ * The first call on a device looks up that device's address of the scratch
+ * array (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture.  All calls share the one array, and each call
+ * overwrites what it needs from it, so calls whose kernels overlap on the GPU
+ * (different streams, or different host threads on the same device) race and
+ * give wrong results: order them on one stream. */
+FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* targets, int64_t T,
+                                          int64_t Hd, int64_t V, int64_t ignore_index, int32_t reduction,
+                                          float* loss, float* lse, float* logp, int64_t* n_valid,
+                                          int32_t* device_status, void* stream);
+
 /* Synchronizes `stream`, then reads the device status word of the latest call
  * made with `workspace` into *out (an flce_status value). */
 FLCE_API flce_status flce_read_device_status(const void* workspace, void* stream, int32_t* out);

@@ -32,6 +32,7 @@ SIGNATURES = {
     "flce_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "flce_backward_chunk_tokens": (_I64, [_I64, _I64, _I64, ctypes.c_size_t]),
     "flce_forward": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_forward_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P]),
     "flce_backward": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "flce_status_string": (ctypes.c_char_p, [_I32]),

@@ -259,6 +259,32 @@ flce_status check_common(const void* H, const void* W, const int64_t* targets, i
   return FLCE_OK;
 }
 
+// ------------------------------------------------------------------ built-in scratch
+// Scratch of flce_forward_noalloc(): a device array of fixed size in this
+// library's module.  Host code must not use the symbol as a pointer; the
+// device address comes from cudaGetSymbolAddress, once per device.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+flce_status static_scratch_address(void** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(FLCE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(FLCE_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed on device %d: %s", dev,
+                  cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return FLCE_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -458,6 +484,27 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
     ks.done();
     if ((st = check_launch("fwd_reduce")) != FLCE_OK) return st;
   }
+  return FLCE_OK;
+}
+
+flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd,
+                                 int64_t V, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
+                                 float* logp, int64_t* n_valid, int32_t* device_status, void* stream) {
+  if (T < 0 || V < 1) return fail(FLCE_ERR_INVALID_ARG, "T = %lld or V = %lld out of range", (long long)T, (long long)V);
+  const size_t need = flce_forward_workspace_size(T, Hd, V);
+  if (need > kStaticScratchBytes)
+    return fail(FLCE_ERR_WORKSPACE,
+                "T = %lld needs %zu bytes of scratch; the built-in scratch holds %zu bytes (T <= 253952)",
+                (long long)T, need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  flce_status st = static_scratch_address(&scratch);
+  if (st != FLCE_OK) return st;
+  st = flce_forward(H, W, targets, T, Hd, V, ignore_index, reduction, loss, lse, logp, n_valid, scratch,
+                    kStaticScratchBytes, stream);
+  if (st != FLCE_OK) return st;
+  if (device_status)
+    CUDA_TRY(cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                             static_cast<cudaStream_t>(stream)));
   return FLCE_OK;
 }
 
