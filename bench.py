@@ -160,7 +160,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     wl = workload(args.workload)
-    inp = generate(wl)
+    inp = generate(wl, T=args.T, Hd=args.Hd, V=args.V)
     W64 = inp.W64()
     for _ in range(args.warmup):
         time_oracle(inp, budget_s=0.0, slice_tokens=32, W64=W64)
@@ -173,9 +173,9 @@ def run_reference(args):
     tokens = value * el
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.T / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * inp.T / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "Hd": wl.Hd, "V": wl.V,
+        "data": "synthetic", "config": {"workload": wl.name, "T": inp.T, "Hd": inp.Hd, "V": inp.V,
                                         "reduction": wl.reduction},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": per[0]["cores"], "kind": "oracle",
                          "sample": f"each step: {per[0]['sample']}"},
@@ -199,7 +199,7 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     wl = workload(args.workload)
-    inp = generate(wl, seed=rank)
+    inp = generate(wl, seed=rank, T=args.T, Hd=args.Hd, V=args.V)
     T, Hd, V = inp.T, inp.Hd, inp.V
     stream = torch.cuda.current_stream(dev)
 
@@ -295,8 +295,7 @@ def run_ours(args):
         return 0
 
     peaks, peak_src = load_peaks()
-    flops_step = 8.0 * T * Hd * V
-    tflops = world * flops_step * args.steps / (ms_total / 1000.0) / 1e12
+    tflops = world * 8.0 * T * Hd * V * args.steps / (ms_total / 1000.0) / 1e12
     dom_name, dom = max(kstats.items(), key=lambda kv: kv[1]["total_ms"])
     avg_ms = dom["total_ms"] / dom["launches"]
     ach = (dom["flops"] / dom["launches"]) / (avg_ms / 1000.0) / 1e12
@@ -310,7 +309,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "Hd": Hd, "V": V, "reduction": wl.reduction,
+        "config": {"workload": wl.name if (T, Hd, V) == (wl.T, wl.Hd, wl.V) else f"{wl.name} at T={T} Hd={Hd} V={V}",
+                   "T": T, "Hd": Hd, "V": V, "reduction": wl.reduction,
                    "backward_chunk_tokens": flce.flce_backward_chunk_tokens(T, Hd, V, bws.numel()),
                    "l2": "inputs larger than L2 (H %.0f MB + W %.0f MB > 129 MB), no flush" % (
                        T * Hd * 2 / 1e6, V * Hd * 2 / 1e6),
@@ -344,6 +344,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--T", type=int, default=None, help="override the workload's token count (same recipe)")
+    ap.add_argument("--Hd", type=int, default=None, help="override the hidden size")
+    ap.add_argument("--V", type=int, default=None, help="override the vocabulary size")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
