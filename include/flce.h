@@ -189,9 +189,8 @@ typedef enum flce_kernel_kind {
   FLCE_KERNEL_FWD_REDUCE = 2,     /* fixed-order scalar loss and n_valid */
   FLCE_KERNEL_BWD_PREP = 3,       /* n_valid and the per-token upstream weights g */
   FLCE_KERNEL_BWD_DZ = 4,         /* recomputed logit tiles + dZ epilogue, bf16 dZ chunk */
-  FLCE_KERNEL_BWD_DH = 5,         /* dH chunk = dZ W */
-  FLCE_KERNEL_BWD_DW = 6,         /* dW += dZ^T H for one chunk */
-  FLCE_KERNEL_KINDS = 7
+  FLCE_KERNEL_BWD_DH_DW = 5,      /* dH chunk = dZ W and dW (+)= dZ^T H, one launch per chunk */
+  FLCE_KERNEL_KINDS = 6
 } flce_kernel_kind;
 
 FLCE_API void flce_profile_enable(int32_t on);

@@ -21,7 +21,7 @@ STATUS_NAMES = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_ALIGNMENT",
     4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
 }
-KERNEL_KINDS = 7
+KERNEL_KINDS = 6
 
 # Every symbol the header declares: name -> (restype, argtypes).
 _P = ctypes.c_void_p

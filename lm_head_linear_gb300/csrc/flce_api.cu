@@ -72,10 +72,8 @@ flce_status device_info(DeviceInfo** out) {
                                   smem_bytes_for(MODE_FWD)));
     CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   smem_bytes_for(MODE_DZ)));
-    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  smem_bytes_for(MODE_DH)));
-    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  smem_bytes_for(MODE_DW)));
+    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DHW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_bytes_for(MODE_DHW)));
     d.attrs_set = true;
   }
   *out = &d;
@@ -200,14 +198,19 @@ FwdLayout fwd_layout(int64_t T, int n_split) {
 struct BwdLayout {
   int64_t chunk;
   int64_t v_pad;
-  size_t g_off, dz_off, total;
+  int64_t max_chunks;
+  size_t cnt_off, g_off, dz_off, total;
 };
 
+// Header | tile counters (one per possible chunk) | g [T] | dZ chunk [chunk, V_pad].
 BwdLayout bwd_layout(int64_t T, int64_t V, int64_t chunk) {
   BwdLayout L{};
   L.chunk = chunk;
   L.v_pad = static_cast<int64_t>(align_up(static_cast<size_t>(V), 64));
+  L.max_chunks = cdiv(std::max<int64_t>(T, 1), 128);
   size_t off = kHeaderBytes;
+  L.cnt_off = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L.max_chunks), 256);
   L.g_off = off;
   off = align_up(off + sizeof(float) * static_cast<size_t>(std::max<int64_t>(T, 1)), 1024);
   L.dz_off = off;
@@ -233,8 +236,8 @@ int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
     const int64_t units = m_blocks * ns;
     const int64_t per_unit = cdiv(n_blocks, ns);
     const int64_t waves = cdiv(units, grid);
-    const double eff = static_cast<double>(m_blocks * n_blocks) /
-                       static_cast<double>(std::min<int64_t>(units, grid) * waves * per_unit);
+    // every SM counts, also those left without a unit
+    const double eff = static_cast<double>(m_blocks * n_blocks) / static_cast<double>(grid * waves * per_unit);
     if (eff > best_eff + 1e-9) {
       best_eff = eff;
       best = ns;
@@ -317,8 +320,7 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_KERNEL_FWD_REDUCE: return "fwd_reduce";
     case FLCE_KERNEL_BWD_PREP: return "bwd_prep";
     case FLCE_KERNEL_BWD_DZ: return "bwd_dz";
-    case FLCE_KERNEL_BWD_DH: return "bwd_dh";
-    case FLCE_KERNEL_BWD_DW: return "bwd_dw";
+    case FLCE_KERNEL_BWD_DH_DW: return "bwd_dh_dw";
     default: return "unknown";
   }
 }
@@ -556,7 +558,12 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
   if ((st = make_map(&tm_dH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dH, Hd, T, Hd * 2, 64, 32)) != FLCE_OK) return st;
   if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
 
-  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
+  const int64_t n_chunks = cdiv(T, chunk);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + L.cnt_off);
+  CUDA_TRY(cudaMemsetAsync(counters, 0, sizeof(int32_t) * static_cast<size_t>(n_chunks), s));
+
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int64_t c0 = c * chunk;
     const int64_t rows = std::min<int64_t>(chunk, T - c0);
     const int64_t m_blocks = cdiv(rows, BM);
     CUtensorMap tm_dz_store, tm_dz_k, tm_dz_mn;
@@ -597,37 +604,28 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
       ks.done();
       if ((st = check_launch("bwd_dz")) != FLCE_OK) return st;
     }
-    // (2) dH rows of the chunk = dZ W
+    // (2) dH rows of the chunk = dZ W and dW (+)= dZ^T H[chunk] in one launch;
+    //     the first chunk stores dW, later chunks add to it, in chunk order.
     p.tmA = tm_dz_k;
     p.tmB = tm_W_mn;
     p.tmOut = tm_dH;
-    p.num_m_blocks = static_cast<int32_t>(m_blocks);
+    p.tmA2 = tm_dz_mn;
+    p.tmB2 = tm_H_mn;
+    p.tmOut2 = tm_dW_out;
     p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
     p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
-    p.num_units = p.num_m_blocks * p.num_n_blocks;
+    p.num_k_blocks2 = static_cast<int32_t>(cdiv(rows, BK));
+    p.n_dh_tiles = static_cast<int32_t>(m_blocks * n_hd_blocks);
+    p.n_dw_tiles = static_cast<int32_t>(cdiv(V, BM) * n_hd_blocks);
+    p.reduce_out = c > 0 ? 1 : 0;
+    p.tile_counter = counters + c;
     {
-      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
-      KernelScope ks(FLCE_KERNEL_BWD_DH, s, 2.0 * rows * Hd * V, 2.0 * rows * V + 2.0 * V * Hd + 2.0 * rows * Hd);
-      gemm_kernel<MODE_DH><<<grid, kThreads, smem_bytes_for(MODE_DH), s>>>(p);
+      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.n_dh_tiles + p.n_dw_tiles));
+      KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 4.0 * rows * Hd * V,
+                     4.0 * rows * V + 2.0 * V * Hd + 4.0 * rows * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd);
+      gemm_kernel<MODE_DHW><<<grid, kThreads, smem_bytes_for(MODE_DHW), s>>>(p);
       ks.done();
-      if ((st = check_launch("bwd_dh")) != FLCE_OK) return st;
-    }
-    // (3) dW (+)= dZ^T H[chunk]; the first chunk stores, later chunks add, in chunk order
-    p.tmA = tm_dz_mn;
-    p.tmB = tm_H_mn;
-    p.tmOut = tm_dW_out;
-    p.num_m_blocks = static_cast<int32_t>(cdiv(V, BM));
-    p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
-    p.num_k_blocks = static_cast<int32_t>(cdiv(rows, BK));
-    p.num_units = p.num_m_blocks * p.num_n_blocks;
-    p.reduce_out = c0 > 0 ? 1 : 0;
-    {
-      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
-      KernelScope ks(FLCE_KERNEL_BWD_DW, s, 2.0 * rows * Hd * V,
-                     2.0 * rows * V + 2.0 * rows * Hd + (c0 > 0 ? 8.0 : 4.0) * V * Hd);
-      gemm_kernel<MODE_DW><<<grid, kThreads, smem_bytes_for(MODE_DW), s>>>(p);
-      ks.done();
-      if ((st = check_launch("bwd_dw")) != FLCE_OK) return st;
+      if ((st = check_launch("bwd_dh_dw")) != FLCE_OK) return st;
     }
   }
   return FLCE_OK;

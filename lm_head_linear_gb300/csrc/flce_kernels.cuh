@@ -11,8 +11,12 @@
 //   MODE_DZ   the same logit tiles recomputed for one token chunk; the
 //             epilogue forms dZ = g (exp(z - lse) - onehot) in registers and
 //             stores it as bf16 into the [chunk x V] dZ slice.
-//   MODE_DH   dH[chunk] = dZ W        (M = tokens, N = Hd, K = vocab)
-//   MODE_DW   dW (+)= dZ^T H[chunk]   (M = vocab,  N = Hd, K = tokens)
+//   MODE_DHW  both contractions of that dZ slice in one launch:
+//               dH[chunk] = dZ W        (M = tokens, N = Hd, K = vocab)
+//               dW (+)= dZ^T H[chunk]   (M = vocab,  N = Hd, K = tokens)
+//             Tiles are handed out by a global atomic counter, the long dH
+//             tiles first, so the short dW tiles fill the SMs that the dH
+//             tiles leave idle at the end of their last wave.
 //
 // CTA layout: 6 warps.  Warp 0: TMA producer (one elected thread).  Warp 1:
 // TMEM allocator and MMA issuer (one elected thread).  Warps 2..5: epilogue;
@@ -45,13 +49,15 @@ constexpr int kEpiWarps = 4;
 constexpr int STAGING_BOX_BYTES = 32 * 128;     // 32 rows x 128 bytes
 constexpr int STAGING_BYTES = kEpiWarps * 2 * STAGING_BOX_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int kBarriers = 2 * NSTAGE + 5;       // full, empty, tmem_full x2, tmem_empty x2, drain
-constexpr int kSmemTail = 256;                  // barriers + TMEM slot + abort flag
+constexpr int kTileRing = 8;                    // MODE_DHW: tile indices in flight inside a CTA
+// full[NSTAGE], empty[NSTAGE], tmem_full[2], tmem_empty[2], drain, tile_full[R], tile_empty[R]
+constexpr int kBarriers = 2 * NSTAGE + 5 + 2 * kTileRing;
+constexpr int kSmemTail = 512;                  // barriers + TMEM slot + abort flag + tile ring
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-enum Mode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DH = 2, MODE_DW = 3 };
+enum Mode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DHW = 2 };
 
 // Device status codes (match flce_status in include/flce.h).
 constexpr int kStatusTargetRange = 6;
@@ -60,29 +66,40 @@ constexpr int kStatusTimeout = 7;
 __host__ __device__ constexpr int smem_bytes_for(int mode) {
   return 1024 + NSTAGE * STAGE_BYTES + (mode == MODE_FWD ? 0 : STAGING_BYTES) + kSmemTail;
 }
+static_assert(smem_bytes_for(MODE_DHW) <= 232448, "shared memory per CTA");
+static_assert(kBarriers * 8 + 8 + kTileRing * 4 <= kSmemTail, "smem tail");
 
 struct GemmParams {
-  CUtensorMap tmA;    // operand A (K-major box {64, 128} or MN-major box {64, 64})
-  CUtensorMap tmB;    // operand B (K-major box {64, 256} or MN-major box {64, 64})
-  CUtensorMap tmOut;  // epilogue store / reduce target (unused by MODE_FWD)
+  // MODE_FWD / MODE_DZ: A = H (K-major), B = W (K-major), tmOut = dZ store.
+  // MODE_DHW dH tiles: A = dZ (K-major), B = W (MN-major), tmOut = dH store.
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  CUtensorMap tmOut;
+  // MODE_DHW dW tiles: A = dZ (MN-major), B = H (MN-major), tmOut2 = dW store / reduce.
+  CUtensorMap tmA2;
+  CUtensorMap tmB2;
+  CUtensorMap tmOut2;
   int32_t num_m_blocks;
   int32_t num_n_blocks;
   int32_t num_k_blocks;
-  int32_t n_split;      // MODE_FWD: vocab ranges per token block
+  int32_t n_split;       // MODE_FWD: vocab ranges per token block
   int32_t num_units;
-  int32_t row0;         // first token of the chunk (0 for MODE_FWD)
-  int32_t rows;         // tokens in the chunk (T for MODE_FWD)
+  int32_t row0;          // first token of the chunk (0 for MODE_FWD)
+  int32_t rows;          // tokens in the chunk (T for MODE_FWD)
   int32_t T;
   int32_t V;
-  int32_t part_stride;  // MODE_FWD: row stride of one split's partials
-  int32_t reduce_out;   // MODE_DW: 0 = store, 1 = reduce-add into the output
-  int32_t pad0;
+  int32_t part_stride;   // MODE_FWD: row stride of one split's partials
+  int32_t reduce_out;    // MODE_DHW: dW tiles 0 = store, 1 = reduce-add into the output
+  int32_t n_dh_tiles;    // MODE_DHW: dH tiles come first in the tile order ...
+  int32_t n_dw_tiles;    // ... then the dW tiles
+  int32_t num_k_blocks2; // MODE_DHW: K blocks of a dW tile (tokens of the chunk / 64)
   int64_t ignore_index;
   const int64_t* targets;
-  const float* lse;     // MODE_DZ
-  const float* g;       // MODE_DZ
-  float2* partials;     // MODE_FWD [n_split][part_stride] of (max*log2e, sum of 2^(z*log2e - max))
-  float* zy;            // MODE_FWD [T] target logit
+  const float* lse;      // MODE_DZ
+  const float* g;        // MODE_DZ
+  float2* partials;      // MODE_FWD [n_split][part_stride] of (max*log2e, sum of 2^(z*log2e - max))
+  float* zy;             // MODE_FWD [T] target logit
+  int32_t* tile_counter; // MODE_DHW: zero before the launch
   int32_t* status;
   uint64_t timeout_ns;
 };
@@ -107,19 +124,32 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
     r.split = split;
     r.n_lo = split * base + min(split, rem);
     r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
-  } else if constexpr (MODE == MODE_DZ) {
+  } else {
     const int nb = u / p.num_m_blocks;  // token blocks fastest: the W tile is shared in L2
     r.m_blk = u - nb * p.num_m_blocks;
     r.n_lo = nb;
     r.n_hi = nb + 1;
     r.split = 0;
-  } else {
-    const int mb = u / p.num_n_blocks;  // Hd blocks fastest: the dZ rows are shared in L2
-    r.m_blk = mb;
-    r.n_lo = u - mb * p.num_n_blocks;
-    r.n_hi = r.n_lo + 1;
-    r.split = 0;
   }
+  return r;
+}
+
+// One MODE_DHW tile: family 0 = dH, family 1 = dW; Hd blocks fastest so that
+// CTAs running side by side share the dZ rows (dH) or dZ columns (dW) in L2.
+struct Tile {
+  int family;
+  int m_blk;
+  int nb;
+  int num_k;
+};
+
+__device__ __forceinline__ Tile decode_dhw(const GemmParams& p, int t) {
+  Tile r;
+  r.family = t < p.n_dh_tiles ? 0 : 1;
+  const int u = r.family ? t - p.n_dh_tiles : t;
+  r.m_blk = u / p.num_n_blocks;
+  r.nb = u - r.m_blk * p.num_n_blocks;
+  r.num_k = r.family ? p.num_k_blocks2 : p.num_k_blocks;
   return r;
 }
 
@@ -131,6 +161,7 @@ struct SmemLayout {
   uint64_t* bars;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  volatile int* tile_ring;
 };
 
 template <int MODE>
@@ -143,6 +174,7 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   s.bars = reinterpret_cast<uint64_t*>(tail);
   s.tmem_slot = reinterpret_cast<uint32_t*>(tail + kBarriers * 8);
   s.abort_flag = reinterpret_cast<volatile int*>(tail + kBarriers * 8 + 4);
+  s.tile_ring = reinterpret_cast<volatile int*>(tail + kBarriers * 8 + 8);
   return s;
 }
 
@@ -157,118 +189,120 @@ __device__ __forceinline__ uint32_t bar_tempty(const SmemLayout& s, int i) {
   return ptx::smem_u32(s.bars + 2 * NSTAGE + 2 + i);
 }
 __device__ __forceinline__ uint32_t bar_drain(const SmemLayout& s) { return ptx::smem_u32(s.bars + 2 * NSTAGE + 4); }
+__device__ __forceinline__ uint32_t bar_tile_full(const SmemLayout& s, int i) {
+  return ptx::smem_u32(s.bars + 2 * NSTAGE + 5 + i);
+}
+__device__ __forceinline__ uint32_t bar_tile_empty(const SmemLayout& s, int i) {
+  return ptx::smem_u32(s.bars + 2 * NSTAGE + 5 + kTileRing + i);
+}
 
 __device__ __forceinline__ void abort_cta(const GemmParams& p, const SmemLayout& s) {
   *s.abort_flag = 1;
   raise_status(p.status, kStatusTimeout);
 }
 
-// ----------------------------------------------------------------------------- producer
-template <int MODE>
-__device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLayout& s) {
-  uint32_t stage = 0, phase = 0;
-  uint32_t issued_mask = 0, issued_parity = 0;
-  bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit un = decode_unit<MODE>(p, u);
-    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-        if (!ptx::wait_bounded(bar_empty(s, stage), phase ^ 1u, p.timeout_ns, s.abort_flag)) {
-          abort_cta(p, s);
-          ok = false;
-          break;
-        }
-        const uint32_t full = bar_full(s, stage);
-        ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
-        const uint32_t a_dst = ptx::smem_u32(s.stages + stage * STAGE_BYTES);
-        const uint32_t b_dst = a_dst + A_BYTES;
-        const int k0 = kb * BK;
-        if constexpr (MODE == MODE_FWD || MODE == MODE_DZ) {
-          ptx::tma_load_2d(a_dst, &p.tmA, k0, p.row0 + un.m_blk * BM, full);
-          ptx::tma_load_2d(b_dst, &p.tmB, k0, nb * BN, full);
-        } else if constexpr (MODE == MODE_DH) {
-          ptx::tma_load_2d(a_dst, &p.tmA, k0, un.m_blk * BM, full);
+// ----------------------------------------------------------------------------- operand loads (one K block)
+// K-major H and W tiles for the logits (forward and recompute).
+__device__ __forceinline__ void load_logits_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst,
+                                                  uint32_t full, int m_blk, int nb, int k0) {
+  ptx::tma_load_2d(a_dst, &p.tmA, k0, p.row0 + m_blk * BM, full);
+  ptx::tma_load_2d(b_dst, &p.tmB, k0, nb * BN, full);
+}
+
+// dH tile: dZ rows (K-major, K = vocab) and W as MN-major 64-column boxes.
+__device__ __forceinline__ void load_dh_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst, uint32_t full,
+                                              int m_blk, int nb, int k0) {
+  ptx::tma_load_2d(a_dst, &p.tmA, k0, m_blk * BM, full);
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) ptx::tma_load_2d(b_dst + j * 8192, &p.tmB, nb * BN + j * 64, k0, full);
-        } else {  // MODE_DW
+  for (int j = 0; j < BN / 64; ++j) ptx::tma_load_2d(b_dst + j * 8192, &p.tmB, nb * BN + j * 64, k0, full);
+}
+
+// dW tile: dZ^T (MN-major 64-vocab boxes, K = tokens) and H[chunk] as MN-major boxes.
+__device__ __forceinline__ void load_dw_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst, uint32_t full,
+                                              int m_blk, int nb, int k0) {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j)
-            ptx::tma_load_2d(a_dst + j * 8192, &p.tmA, un.m_blk * BM + j * 64, k0, full);
+  for (int j = 0; j < BM / 64; ++j) ptx::tma_load_2d(a_dst + j * 8192, &p.tmA2, m_blk * BM + j * 64, k0, full);
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            ptx::tma_load_2d(b_dst + j * 8192, &p.tmB, nb * BN + j * 64, p.row0 + k0, full);
-        }
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == NSTAGE) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+  for (int j = 0; j < BN / 64; ++j) ptx::tma_load_2d(b_dst + j * 8192, &p.tmB2, nb * BN + j * 64, p.row0 + k0, full);
+}
+
+// Ring bookkeeping of the producer: which stages hold loads, and their phase.
+struct ProducerState {
+  uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
+  __device__ __forceinline__ void advance() {
+    issued_mask |= 1u << stage;
+    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+    if (++stage == NSTAGE) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
   // Never leave the CTA with TMA writes into its shared memory in flight.
-  for (int i = 0; i < NSTAGE; ++i)
-    if (issued_mask & (1u << i))
-      ptx::wait_bounded(bar_full(s, i), (issued_parity >> i) & 1u, kDrainTimeoutNs, nullptr);
+  __device__ __forceinline__ void drain(const SmemLayout& s) const {
+    for (int i = 0; i < NSTAGE; ++i)
+      if (issued_mask & (1u << i))
+        ptx::wait_bounded(bar_full(s, i), (issued_parity >> i) & 1u, kDrainTimeoutNs, nullptr);
+  }
+};
+
+// Loads the K blocks of one tile; `kind` 0 = logits, 1 = dH, 2 = dW.
+__device__ __forceinline__ bool produce_tile(const GemmParams& p, const SmemLayout& s, ProducerState& ps, int kind,
+                                             int m_blk, int nb, int num_k) {
+  for (int kb = 0; kb < num_k; ++kb) {
+    if (!ptx::wait_bounded(bar_empty(s, ps.stage), ps.phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      return false;
+    }
+    const uint32_t full = bar_full(s, ps.stage);
+    ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+    const uint32_t a_dst = ptx::smem_u32(s.stages + ps.stage * STAGE_BYTES);
+    const uint32_t b_dst = a_dst + A_BYTES;
+    const int k0 = kb * BK;
+    if (kind == 0)
+      load_logits_stage(p, a_dst, b_dst, full, m_blk, nb, k0);
+    else if (kind == 1)
+      load_dh_stage(p, a_dst, b_dst, full, m_blk, nb, k0);
+    else
+      load_dw_stage(p, a_dst, b_dst, full, m_blk, nb, k0);
+    ps.advance();
+  }
+  return true;
 }
 
-// ----------------------------------------------------------------------------- MMA issuer
-template <int MODE>
-__device__ __forceinline__ void mma_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
-  constexpr uint32_t a_mn = (MODE == MODE_DW) ? 1u : 0u;
-  constexpr uint32_t b_mn = (MODE == MODE_DH || MODE == MODE_DW) ? 1u : 0u;
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, a_mn, b_mn);
-  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-  bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit un = decode_unit<MODE>(p, u);
-    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
-      if (!ptx::wait_bounded(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
-        abort_cta(p, s);
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-        if (!ptx::wait_bounded(bar_full(s, stage), phase, p.timeout_ns, s.abort_flag)) {
-          abort_cta(p, s);
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_u32(s.stages + stage * STAGE_BYTES);
-        const uint32_t b_addr = a_addr + A_BYTES;
+// ----------------------------------------------------------------------------- MMA (one tile)
+// Issues the K loop of one tile into the accumulator at d_tmem.  K-major
+// operand: the 16-deep slice is 32 bytes further along the swizzled 128-byte
+// row, 8-row groups 1024 bytes apart.  MN-major operand: the slice is 16 rows
+// (2048 bytes) further, 64-wide MN blocks 8 KB apart.
+__device__ __forceinline__ bool mma_tile(const GemmParams& p, const SmemLayout& s, uint32_t d_tmem, int num_k,
+                                         uint32_t a_mn, uint32_t b_mn, uint32_t idesc, uint32_t& stage,
+                                         uint32_t& phase) {
+  for (int kb = 0; kb < num_k; ++kb) {
+    if (!ptx::wait_bounded(bar_full(s, stage), phase, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      return false;
+    }
+    ptx::tc_fence_after();
+    const uint32_t a_addr = ptx::smem_u32(s.stages + stage * STAGE_BYTES);
+    const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          // K-major: the 16-deep slice is 32 bytes further along the swizzled
-          // 128-byte row; 8-row groups are 1024 bytes apart.  MN-major: the
-          // slice is 16 rows (2048 bytes) further; 64-wide MN blocks are 8 KB apart.
-          const uint64_t a_desc = a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
-                                       : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          const uint64_t b_desc = b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                       : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
-          ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(bar_empty(s, stage));
-        if (++stage == NSTAGE) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
-      ptx::mma_commit(bar_tfull(s, acc));
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+    for (int k = 0; k < BK / 16; ++k) {
+      const uint64_t a_desc = a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                   : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+      const uint64_t b_desc = b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                   : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+      ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
+    }
+    ptx::mma_commit(bar_empty(s, stage));
+    if (++stage == NSTAGE) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
-  // Wait for every MMA issued so far before TMEM is freed.
-  ptx::mma_commit(bar_drain(s));
-  ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
+  return true;
 }
 
-// ----------------------------------------------------------------------------- epilogues
+// ----------------------------------------------------------------------------- epilogue pieces
 // TMEM load of 32 columns for this warp's 32 rows, completed before return.
 __device__ __forceinline__ void tmem_load32_sync(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -288,6 +322,111 @@ __device__ __forceinline__ void stage_row_words(uint32_t buf, int lane, const ui
     ptx::st_shared_v4(row + ((k ^ (lane & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
+// Stages one 32-row x 128-byte box in a staging buffer (alternating two per
+// warp) and stores or reduce-adds it with TMA at (x, yrow).
+__device__ __forceinline__ void store_box(const CUtensorMap* tm, bool reduce, uint32_t staging0,
+                                          uint32_t& box_count, int lane, const uint32_t (&w)[32], int x, int yrow) {
+  const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
+  if (lane == 0) ptx::bulk_wait_read<1>();
+  __syncwarp();
+  stage_row_words(buf, lane, w);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (reduce)
+      ptx::tma_reduce_add_2d(tm, buf, x, yrow);
+    else
+      ptx::tma_store_2d(tm, buf, x, yrow);
+    ptx::bulk_commit();
+  }
+  ++box_count;
+}
+
+// bf16 tile store (dZ or dH): 4 boxes of 64 columns.  With DZ set, each
+// accumulator value z becomes g (2^(z log2e - lse log2e) - [col == y]).
+template <bool DZ>
+__device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tcol, int x0, int yrow,
+                                              uint32_t staging0, uint32_t& box_count, int lane, float gt,
+                                              float lse2, int y) {
+#pragma unroll 1
+  for (int j = 0; j < BN / 64; ++j) {
+    uint32_t w[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float v[32];
+      tmem_load32_sync(tcol + j * 64 + h * 32, v);
+      if constexpr (DZ) {
+        const int col0 = x0 + j * 64 + h * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = ptx::ex2(fmaf(v[i], kLog2e, -lse2));
+        const int yo = y - col0;
+        if (static_cast<unsigned>(yo) < 32u) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i == yo) v[i] -= 1.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= gt;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[h * 16 + i] = ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+    store_box(tm, false, staging0, box_count, lane, w, x0 + j * 64, yrow);
+  }
+}
+
+// fp32 tile store or reduce-add (dW): 8 boxes of 32 columns.
+__device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce, uint32_t tcol, int x0, int yrow,
+                                             uint32_t staging0, uint32_t& box_count, int lane) {
+#pragma unroll 1
+  for (int j = 0; j < BN / 32; ++j) {
+    float v[32];
+    tmem_load32_sync(tcol + j * 32, v);
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+    store_box(tm, reduce, staging0, box_count, lane, w, x0 + j * 32, yrow);
+  }
+}
+
+// ----------------------------------------------------------------------------- MODE_FWD / MODE_DZ loops (static schedule)
+template <int MODE>
+__device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLayout& s) {
+  ProducerState ps;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    const Unit un = decode_unit<MODE>(p, u);
+    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) ok = produce_tile(p, s, ps, 0, un.m_blk, nb, p.num_k_blocks);
+  }
+  ps.drain(s);
+}
+
+template <int MODE>
+__device__ __forceinline__ void mma_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, 0, 0);
+  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    const Unit un = decode_unit<MODE>(p, u);
+    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
+      if (!ptx::wait_bounded(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+        abort_cta(p, s);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      ok = mma_tile(p, s, tmem_base + acc * BN, p.num_k_blocks, 0, 0, idesc, stage, phase);
+      if (!ok) break;
+      ptx::mma_commit(bar_tfull(s, acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  // Wait for every MMA issued so far before TMEM is freed.
+  ptx::mma_commit(bar_drain(s));
+  ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base,
                                               int warp, int lane) {
@@ -295,13 +434,13 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
   const int row_in_tile = q * 32 + lane;
   const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   uint32_t acc = 0, acc_phase = 0;
-  uint32_t box_count = 0;  // staging buffers alternate per stored box
+  uint32_t box_count = 0;
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
   bool ok = true;
 
   for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
     const Unit un = decode_unit<MODE>(p, u);
-    const int t_local = un.m_blk * BM + row_in_tile;  // M index within the launch
+    const int t_local = un.m_blk * BM + row_in_tile;  // token within the launch
 
     float m_run = -INFINITY, s_run = 0.0f, zy = 0.0f;
     bool have_zy = false;
@@ -312,7 +451,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
         const int64_t yy = p.targets[t_local];
         if (yy != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
       }
-    } else if constexpr (MODE == MODE_DZ) {
+    } else {
       if (t_local < p.rows) {
         const int t = p.row0 + t_local;
         gt = p.g[t];
@@ -360,69 +499,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
           s_run = s_run * ptx::ex2(m_run - m_new) + acc_s;
           m_run = m_new;
         }
-      } else if constexpr (MODE == MODE_DZ || MODE == MODE_DH) {
-#pragma unroll 1
-        for (int j = 0; j < BN / 64; ++j) {
-          uint32_t w[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[32];
-            tmem_load32_sync(tcol + j * 64 + h * 32, v);
-            if constexpr (MODE == MODE_DZ) {
-              const int col0 = nb * BN + j * 64 + h * 32;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = ptx::ex2(fmaf(v[i], kLog2e, -lse2));
-              const int yo = y - col0;
-              if (static_cast<unsigned>(yo) < 32u) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i == yo) v[i] -= 1.0f;
-              }
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= gt;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[h * 16 + i] = ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          }
-          const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
-          if (lane == 0) ptx::bulk_wait_read<1>();
-          __syncwarp();
-          stage_row_words(buf, lane, w);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int x = nb * BN + j * 64;
-            const int yrow = (MODE == MODE_DZ ? 0 : p.row0) + un.m_blk * BM + q * 32;
-            ptx::tma_store_2d(&p.tmOut, buf, x, yrow);
-            ptx::bulk_commit();
-          }
-          ++box_count;
-        }
-      } else {  // MODE_DW: fp32 boxes of 32 columns
-#pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
-          float v[32];
-          tmem_load32_sync(tcol + j * 32, v);
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
-          const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
-          if (lane == 0) ptx::bulk_wait_read<1>();
-          __syncwarp();
-          stage_row_words(buf, lane, w);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int x = nb * BN + j * 32;
-            const int yrow = un.m_blk * BM + q * 32;
-            if (p.reduce_out)
-              ptx::tma_reduce_add_2d(&p.tmOut, buf, x, yrow);
-            else
-              ptx::tma_store_2d(&p.tmOut, buf, x, yrow);
-            ptx::bulk_commit();
-          }
-          ++box_count;
-        }
+      } else {
+        epi_bf16_tile<true>(&p.tmOut, tcol, nb * BN, un.m_blk * BM + q * 32, staging0, box_count, lane, gt, lse2, y);
       }
 
       ptx::tc_fence_before();
@@ -438,6 +516,104 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
         if (have_zy) p.zy[t_local] = zy;
       }
     }
+  }
+  if (lane == 0) ptx::bulk_wait<0>();
+  __syncwarp();
+}
+
+// ----------------------------------------------------------------------------- MODE_DHW loops (dynamic schedule)
+// The producer takes the next tile index from the global counter and passes
+// it to the MMA thread and the epilogue warps through a ring of kTileRing
+// slots in shared memory (tile_full: published; tile_empty: read by all five
+// consumers).  An index >= the tile count ends every role's loop.
+__device__ __forceinline__ void dhw_producer(const GemmParams& p, const SmemLayout& s) {
+  ProducerState ps;
+  const int total = p.n_dh_tiles + p.n_dw_tiles;
+  for (int i = 0;; ++i) {
+    const int slot = i % kTileRing;
+    const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
+    if (!ptx::wait_bounded(bar_tile_empty(s, slot), ph ^ 1u, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      break;
+    }
+    const int t = atomicAdd(p.tile_counter, 1);
+    s.tile_ring[slot] = t;
+    ptx::mbar_arrive(bar_tile_full(s, slot));
+    if (t >= total) break;
+    const Tile ti = decode_dhw(p, t);
+    if (!produce_tile(p, s, ps, 1 + ti.family, ti.m_blk, ti.nb, ti.num_k)) break;
+  }
+  ps.drain(s);
+}
+
+__device__ __forceinline__ void dhw_mma(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
+  constexpr uint32_t idesc_dh = ptx::idesc_bf16_f32(BM, BN, 0, 1);
+  constexpr uint32_t idesc_dw = ptx::idesc_bf16_f32(BM, BN, 1, 1);
+  const int total = p.n_dh_tiles + p.n_dw_tiles;
+  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  for (int i = 0;; ++i) {
+    const int slot = i % kTileRing;
+    const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
+    if (!ptx::wait_bounded(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      break;
+    }
+    const int t = s.tile_ring[slot];
+    ptx::mbar_arrive(bar_tile_empty(s, slot));
+    if (t >= total) break;
+    const Tile ti = decode_dhw(p, t);
+    if (!ptx::wait_bounded(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      break;
+    }
+    ptx::tc_fence_after();
+    if (!mma_tile(p, s, tmem_base + acc * BN, ti.num_k, static_cast<uint32_t>(ti.family), 1u,
+                  ti.family ? idesc_dw : idesc_dh, stage, phase))
+      break;
+    ptx::mma_commit(bar_tfull(s, acc));
+    acc ^= 1u;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  ptx::mma_commit(bar_drain(s));
+  ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
+}
+
+__device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base, int warp,
+                                             int lane) {
+  const int q = warp & 3;
+  const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
+  const int total = p.n_dh_tiles + p.n_dw_tiles;
+  uint32_t acc = 0, acc_phase = 0, box_count = 0;
+  for (int i = 0;; ++i) {
+    const int slot = i % kTileRing;
+    const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
+    if (!ptx::wait_bounded(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      break;
+    }
+    const int t = s.tile_ring[slot];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_tile_empty(s, slot));
+    if (t >= total) break;
+    const Tile ti = decode_dhw(p, t);
+    if (!ptx::wait_bounded(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      break;
+    }
+    ptx::tc_fence_after();
+    const uint32_t tcol = lane_addr + acc * BN;
+    if (ti.family == 0)
+      epi_bf16_tile<false>(&p.tmOut, tcol, ti.nb * BN, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count, lane,
+                           0.0f, 0.0f, -1);
+    else
+      epi_f32_tile(&p.tmOut2, p.reduce_out != 0, tcol, ti.nb * BN, ti.m_blk * BM + q * 32, staging0, box_count,
+                   lane);
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_tempty(s, acc));
+    acc ^= 1u;
+    if (acc == 0) acc_phase ^= 1u;
   }
   if (lane == 0) ptx::bulk_wait<0>();
   __syncwarp();
@@ -461,6 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       ptx::mbar_init(bar_tempty(s, i), kEpiWarps);
     }
     ptx::mbar_init(bar_drain(s), 1);
+    for (int i = 0; i < kTileRing; ++i) {
+      ptx::mbar_init(bar_tile_full(s, i), 1);
+      ptx::mbar_init(bar_tile_empty(s, i), 1 + kEpiWarps);
+    }
     *s.abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
@@ -469,6 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     ptx::prefetch_tmap(&p.tmA);
     ptx::prefetch_tmap(&p.tmB);
     if (MODE != MODE_FWD) ptx::prefetch_tmap(&p.tmOut);
+    if (MODE == MODE_DHW) {
+      ptx::prefetch_tmap(&p.tmA2);
+      ptx::prefetch_tmap(&p.tmB2);
+      ptx::prefetch_tmap(&p.tmOut2);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), TMEM_COLS);
@@ -480,13 +665,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const uint32_t tmem_base = *s.tmem_slot;
 
   if (warp == 0) {
-    if (ptx::elect_one()) producer_loop<MODE>(p, s);
+    if (ptx::elect_one()) {
+      if constexpr (MODE == MODE_DHW)
+        dhw_producer(p, s);
+      else
+        producer_loop<MODE>(p, s);
+    }
     __syncwarp();
   } else if (warp == 1) {
-    if (ptx::elect_one()) mma_loop<MODE>(p, s, tmem_base);
+    if (ptx::elect_one()) {
+      if constexpr (MODE == MODE_DHW)
+        dhw_mma(p, s, tmem_base);
+      else
+        mma_loop<MODE>(p, s, tmem_base);
+    }
     __syncwarp();
   } else {
-    epilogue_loop<MODE>(p, s, tmem_base, warp, lane);
+    if constexpr (MODE == MODE_DHW)
+      dhw_epilogue(p, s, tmem_base, warp, lane);
+    else
+      epilogue_loop<MODE>(p, s, tmem_base, warp, lane);
   }
 
   ptx::tc_fence_before();
