@@ -49,7 +49,20 @@ struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
   bool attrs_set = false;
+  int pairs[3] = {0, 0, 0};  // co-resident CTA pairs (clusters of 2) per GEMM mode
 };
+
+template <int MODE>
+flce_status query_pairs(DeviceInfo& d) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * std::max(d.sms / 2, 1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes_for(MODE);
+  int n = 0;
+  CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, gemm_kernel<MODE>, &cfg));
+  d.pairs[MODE] = std::max(1, std::min(n, d.sms / 2));
+  return FLCE_OK;
+}
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
 
@@ -74,6 +87,10 @@ flce_status device_info(DeviceInfo** out) {
                                   smem_bytes_for(MODE_DZ)));
     CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DHW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   smem_bytes_for(MODE_DHW)));
+    flce_status st;
+    if ((st = query_pairs<MODE_FWD>(d)) != FLCE_OK) return st;
+    if ((st = query_pairs<MODE_DZ>(d)) != FLCE_OK) return st;
+    if ((st = query_pairs<MODE_DHW>(d)) != FLCE_OK) return st;
     d.attrs_set = true;
   }
   *out = &d;
@@ -423,20 +440,20 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
     return FLCE_OK;
   }
 
-  const int64_t m_blocks = cdiv(T, BM);
+  const int64_t m_pairs = cdiv(T, 2 * BM);
   const int64_t n_blocks = cdiv(V, BN);
-  const int n_split = pick_split(m_blocks, n_blocks, dev->sms);
+  const int n_split = pick_split(m_pairs, n_blocks, dev->pairs[MODE_FWD]);
   const FwdLayout L = fwd_layout(T, n_split);
 
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   if ((st = make_map(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
-  if ((st = make_map(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN)) != FLCE_OK) return st;
-  p.num_m_blocks = static_cast<int32_t>(m_blocks);
+  if ((st = make_map(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
+  p.num_m_pairs = static_cast<int32_t>(m_pairs);
   p.num_n_blocks = static_cast<int32_t>(n_blocks);
   p.num_k_blocks = static_cast<int32_t>(Hd / BK);
   p.n_split = n_split;
-  p.num_units = static_cast<int32_t>(m_blocks * n_split);
+  p.num_units = static_cast<int32_t>(m_pairs * n_split);
   p.row0 = 0;
   p.rows = static_cast<int32_t>(T);
   p.T = static_cast<int32_t>(T);
@@ -452,7 +469,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
   const double mma_flops = 2.0 * T * Hd * V;
   const double in_bytes = 2.0 * (T * Hd + V * Hd);
   {
-    const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
+    const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_FWD], p.num_units));
     KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, mma_flops, in_bytes + 8.0 * n_split * T + 4.0 * T);
     gemm_kernel<MODE_FWD><<<grid, kThreads, smem_bytes_for(MODE_FWD), s>>>(p);
     ks.done();
@@ -552,7 +569,7 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
   const int64_t n_hd_blocks = cdiv(Hd, BN);
   CUtensorMap tm_H_k, tm_W_k, tm_W_mn, tm_H_mn, tm_dH, tm_dW_out;
   if ((st = make_map(&tm_H_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
   if ((st = make_map(&tm_W_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, 64, 64)) != FLCE_OK) return st;
   if ((st = make_map(&tm_H_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, 64, 64)) != FLCE_OK) return st;
   if ((st = make_map(&tm_dH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dH, Hd, T, Hd * 2, 64, 32)) != FLCE_OK) return st;
@@ -565,7 +582,7 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
   for (int64_t c = 0; c < n_chunks; ++c) {
     const int64_t c0 = c * chunk;
     const int64_t rows = std::min<int64_t>(chunk, T - c0);
-    const int64_t m_blocks = cdiv(rows, BM);
+    const int64_t m_pairs = cdiv(rows, 2 * BM);
     CUtensorMap tm_dz_store, tm_dz_k, tm_dz_mn;
     if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 32)) != FLCE_OK)
       return st;
@@ -592,12 +609,12 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
     p.tmA = tm_H_k;
     p.tmB = tm_W_k;
     p.tmOut = tm_dz_store;
-    p.num_m_blocks = static_cast<int32_t>(m_blocks);
+    p.num_m_pairs = static_cast<int32_t>(m_pairs);
     p.num_n_blocks = static_cast<int32_t>(cdiv(V, BN));
     p.num_k_blocks = static_cast<int32_t>(Hd / BK);
-    p.num_units = p.num_m_blocks * p.num_n_blocks;
+    p.num_units = p.num_m_pairs * p.num_n_blocks;
     {
-      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.num_units));
+      const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DZ], p.num_units));
       KernelScope ks(FLCE_KERNEL_BWD_DZ, s, 2.0 * rows * Hd * V,
                      2.0 * (rows * Hd + V * Hd) + 2.0 * rows * V + 16.0 * rows);
       gemm_kernel<MODE_DZ><<<grid, kThreads, smem_bytes_for(MODE_DZ), s>>>(p);
@@ -615,12 +632,12 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
     p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
     p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
     p.num_k_blocks2 = static_cast<int32_t>(cdiv(rows, BK));
-    p.n_dh_tiles = static_cast<int32_t>(m_blocks * n_hd_blocks);
-    p.n_dw_tiles = static_cast<int32_t>(cdiv(V, BM) * n_hd_blocks);
+    p.n_dh_tiles = static_cast<int32_t>(m_pairs * n_hd_blocks);
+    p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
     p.reduce_out = c > 0 ? 1 : 0;
     p.tile_counter = counters + c;
     {
-      const int grid = static_cast<int>(std::min<int64_t>(dev->sms, p.n_dh_tiles + p.n_dw_tiles));
+      const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DHW], p.n_dh_tiles + p.n_dw_tiles));
       KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 4.0 * rows * Hd * V,
                      4.0 * rows * V + 2.0 * V * Hd + 4.0 * rows * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd);
       gemm_kernel<MODE_DHW><<<grid, kThreads, smem_bytes_for(MODE_DHW), s>>>(p);

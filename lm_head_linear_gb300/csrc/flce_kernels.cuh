@@ -18,15 +18,26 @@
 //             tiles first, so the short dW tiles fill the SMs that the dH
 //             tiles leave idle at the end of their last wave.
 //
-// CTA layout: 6 warps.  Warp 0: TMA producer (one elected thread).  Warp 1:
-// TMEM allocator and MMA issuer (one elected thread).  Warps 2..5: epilogue;
-// warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows 32*(w%4) .. +31.
+// SM pairs: every kernel runs as clusters of two CTAs on two SMs that compute
+// one 256 x 256 output tile together with cta_group::2 MMAs (M = 256, N = 256,
+// K = 16).  CTA rank r of the pair stages rows 128*r .. +127 of the A tile and
+// rows 128*r .. +127 of the B tile (B's N dimension) in its own shared memory;
+// the tensor cores of the pair read both halves, so each SM streams half of B
+// instead of all of it.  Rank r's TMEM holds rows 128*r .. +127 of the fp32
+// accumulator (all 256 columns).
 //
-// Tiles are 128 x 256 with 64-deep K blocks: one bf16 K block of a row is
-// 128 bytes, the width of the 128-byte TMA / UMMA swizzle.  Operand tiles pass
-// through a ring of NSTAGE shared-memory stages; the fp32 accumulator lives in
-// TMEM, double-buffered (2 x 256 columns) so that the epilogue of one tile
-// overlaps the MMAs of the next.
+// CTA layout: 6 warps per CTA.  Warp 0: TMA producer (one elected thread) in
+// both CTAs; their loads are counted on the even CTA's stage barrier.  Warp 1:
+// TMEM allocator in both CTAs; in the even CTA also the MMA issuer (one
+// elected thread), whose commits arrive on the barriers of both CTAs.  Warps
+// 2..5: epilogue; warp w reads TMEM lanes 32*(w%4) .. +31 of its own CTA and
+// signals the even CTA when the accumulator may be overwritten.
+//
+// K blocks are 64 deep: one bf16 K block of a row is 128 bytes, the width of
+// the 128-byte TMA / UMMA swizzle.  Operand halves pass through a ring of
+// NSTAGE shared-memory stages; the accumulator is double-buffered in TMEM
+// (2 x 256 columns) so that the epilogue of one tile overlaps the MMAs of the
+// next.
 #pragma once
 
 #include <cstdint>
@@ -37,13 +48,15 @@
 
 namespace flce {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;                         // tile rows held by one CTA (the pair MMA has M = 256)
+constexpr int BN = 256;                         // N of the pair MMA
+constexpr int BN_HALF = BN / 2;                 // rows of B staged by each CTA of the pair
 constexpr int BK = 64;
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE = 6;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
+constexpr uint32_t PAIR_TX_BYTES = 2 * STAGE_BYTES;  // both CTAs' loads of a stage
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int STAGING_BOX_BYTES = 32 * 128;     // 32 rows x 128 bytes
@@ -79,7 +92,7 @@ struct GemmParams {
   CUtensorMap tmA2;
   CUtensorMap tmB2;
   CUtensorMap tmOut2;
-  int32_t num_m_blocks;
+  int32_t num_m_pairs;   // 256-row tile pairs along M (tokens); MODE_DHW: dH tiles
   int32_t num_n_blocks;
   int32_t num_k_blocks;
   int32_t n_split;       // MODE_FWD: vocab ranges per token block
@@ -111,22 +124,23 @@ struct Unit {
   int split;
 };
 
+// Work unit of a pair; m_blk is this CTA's 128-row block (2 * pair + rank).
 template <int MODE>
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, uint32_t rank) {
   Unit r;
   if constexpr (MODE == MODE_FWD) {
-    // split-major order: CTAs running side by side share a vocab range, so
+    // split-major order: pairs running side by side share a vocab range, so
     // they walk the same W tiles at about the same time and reuse them in L2.
-    const int split = u / p.num_m_blocks;
+    const int split = u / p.num_m_pairs;
     const int base = p.num_n_blocks / p.n_split;
     const int rem = p.num_n_blocks % p.n_split;
-    r.m_blk = u - split * p.num_m_blocks;
+    r.m_blk = 2 * (u - split * p.num_m_pairs) + static_cast<int>(rank);
     r.split = split;
     r.n_lo = split * base + min(split, rem);
     r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
   } else {
-    const int nb = u / p.num_m_blocks;  // token blocks fastest: the W tile is shared in L2
-    r.m_blk = u - nb * p.num_m_blocks;
+    const int nb = u / p.num_m_pairs;  // token blocks fastest: the W tile is shared in L2
+    r.m_blk = 2 * (u - nb * p.num_m_pairs) + static_cast<int>(rank);
     r.n_lo = nb;
     r.n_hi = nb + 1;
     r.split = 0;
@@ -143,12 +157,13 @@ struct Tile {
   int num_k;
 };
 
-__device__ __forceinline__ Tile decode_dhw(const GemmParams& p, int t) {
+__device__ __forceinline__ Tile decode_dhw(const GemmParams& p, int t, uint32_t rank) {
   Tile r;
   r.family = t < p.n_dh_tiles ? 0 : 1;
   const int u = r.family ? t - p.n_dh_tiles : t;
-  r.m_blk = u / p.num_n_blocks;
-  r.nb = u - r.m_blk * p.num_n_blocks;
+  const int pair = u / p.num_n_blocks;
+  r.nb = u - pair * p.num_n_blocks;
+  r.m_blk = 2 * pair + static_cast<int>(rank);
   r.num_k = r.family ? p.num_k_blocks2 : p.num_k_blocks;
   return r;
 }
@@ -202,28 +217,34 @@ __device__ __forceinline__ void abort_cta(const GemmParams& p, const SmemLayout&
 }
 
 // ----------------------------------------------------------------------------- operand loads (one K block)
-// K-major H and W tiles for the logits (forward and recompute).
+// Each CTA of the pair loads its A rows (its m_blk) and its half of B (N rows
+// nb*256 + 128*rank ..); `full` is the even CTA's stage barrier, as a
+// shared::cluster address, which counts the bytes of both CTAs.
+// K-major H and W for the logits (forward and recompute).
 __device__ __forceinline__ void load_logits_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst,
-                                                  uint32_t full, int m_blk, int nb, int k0) {
-  ptx::tma_load_2d(a_dst, &p.tmA, k0, p.row0 + m_blk * BM, full);
-  ptx::tma_load_2d(b_dst, &p.tmB, k0, nb * BN, full);
+                                                  uint32_t full, int m_blk, int nb, int k0, uint32_t rank) {
+  ptx::tma_load_2d_pair(a_dst, &p.tmA, k0, p.row0 + m_blk * BM, full);
+  ptx::tma_load_2d_pair(b_dst, &p.tmB, k0, nb * BN + static_cast<int>(rank) * BN_HALF, full);
 }
 
 // dH tile: dZ rows (K-major, K = vocab) and W as MN-major 64-column boxes.
 __device__ __forceinline__ void load_dh_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst, uint32_t full,
-                                              int m_blk, int nb, int k0) {
-  ptx::tma_load_2d(a_dst, &p.tmA, k0, m_blk * BM, full);
+                                              int m_blk, int nb, int k0, uint32_t rank) {
+  ptx::tma_load_2d_pair(a_dst, &p.tmA, k0, m_blk * BM, full);
 #pragma unroll
-  for (int j = 0; j < BN / 64; ++j) ptx::tma_load_2d(b_dst + j * 8192, &p.tmB, nb * BN + j * 64, k0, full);
+  for (int j = 0; j < BN_HALF / 64; ++j)
+    ptx::tma_load_2d_pair(b_dst + j * 8192, &p.tmB, nb * BN + static_cast<int>(rank) * BN_HALF + j * 64, k0, full);
 }
 
 // dW tile: dZ^T (MN-major 64-vocab boxes, K = tokens) and H[chunk] as MN-major boxes.
 __device__ __forceinline__ void load_dw_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst, uint32_t full,
-                                              int m_blk, int nb, int k0) {
+                                              int m_blk, int nb, int k0, uint32_t rank) {
 #pragma unroll
-  for (int j = 0; j < BM / 64; ++j) ptx::tma_load_2d(a_dst + j * 8192, &p.tmA2, m_blk * BM + j * 64, k0, full);
+  for (int j = 0; j < BM / 64; ++j) ptx::tma_load_2d_pair(a_dst + j * 8192, &p.tmA2, m_blk * BM + j * 64, k0, full);
 #pragma unroll
-  for (int j = 0; j < BN / 64; ++j) ptx::tma_load_2d(b_dst + j * 8192, &p.tmB2, nb * BN + j * 64, p.row0 + k0, full);
+  for (int j = 0; j < BN_HALF / 64; ++j)
+    ptx::tma_load_2d_pair(b_dst + j * 8192, &p.tmB2, nb * BN + static_cast<int>(rank) * BN_HALF + j * 64,
+                          p.row0 + k0, full);
 }
 
 // Ring bookkeeping of the producer: which stages hold loads, and their phase.
@@ -237,8 +258,11 @@ struct ProducerState {
       phase ^= 1u;
     }
   }
-  // Never leave the CTA with TMA writes into its shared memory in flight.
-  __device__ __forceinline__ void drain(const SmemLayout& s) const {
+  // The even CTA's stage barriers count both CTAs' loads: waiting on the
+  // last-armed phase of each stage means no TMA write of either CTA is in
+  // flight.  (The odd CTA's loads are consumed by the same MMAs.)
+  __device__ __forceinline__ void drain(const SmemLayout& s, uint32_t rank) const {
+    if (rank != 0) return;
     for (int i = 0; i < NSTAGE; ++i)
       if (issued_mask & (1u << i))
         ptx::wait_bounded(bar_full(s, i), (issued_parity >> i) & 1u, kDrainTimeoutNs, nullptr);
@@ -247,30 +271,33 @@ struct ProducerState {
 
 // Loads the K blocks of one tile; `kind` 0 = logits, 1 = dH, 2 = dW.
 __device__ __forceinline__ bool produce_tile(const GemmParams& p, const SmemLayout& s, ProducerState& ps, int kind,
-                                             int m_blk, int nb, int num_k) {
+                                             int m_blk, int nb, int num_k, uint32_t rank) {
   for (int kb = 0; kb < num_k; ++kb) {
-    if (!ptx::wait_bounded(bar_empty(s, ps.stage), ps.phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+    if (!ptx::wait_bounded_cluster(bar_empty(s, ps.stage), ps.phase ^ 1u, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       return false;
     }
-    const uint32_t full = bar_full(s, ps.stage);
-    ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+    const uint32_t full_local = bar_full(s, ps.stage);
+    if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, PAIR_TX_BYTES);
+    const uint32_t full = ptx::mapa(full_local, 0);
     const uint32_t a_dst = ptx::smem_u32(s.stages + ps.stage * STAGE_BYTES);
     const uint32_t b_dst = a_dst + A_BYTES;
     const int k0 = kb * BK;
     if (kind == 0)
-      load_logits_stage(p, a_dst, b_dst, full, m_blk, nb, k0);
+      load_logits_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
     else if (kind == 1)
-      load_dh_stage(p, a_dst, b_dst, full, m_blk, nb, k0);
+      load_dh_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
     else
-      load_dw_stage(p, a_dst, b_dst, full, m_blk, nb, k0);
+      load_dw_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
     ps.advance();
   }
   return true;
 }
 
 // ----------------------------------------------------------------------------- MMA (one tile)
-// Issues the K loop of one tile into the accumulator at d_tmem.  K-major
+// Issues the K loop of one pair tile into the accumulator at d_tmem (rows
+// 0..127 in the even CTA's TMEM, 128..255 in the odd CTA's); each stage is
+// released to both CTAs' producers when its MMAs complete.  K-major
 // operand: the 16-deep slice is 32 bytes further along the swizzled 128-byte
 // row, 8-row groups 1024 bytes apart.  MN-major operand: the slice is 16 rows
 // (2048 bytes) further, 64-wide MN blocks 8 KB apart.
@@ -291,9 +318,9 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const SmemLayout& 
                                    : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
       const uint64_t b_desc = b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                    : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
-      ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
+      ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
     }
-    ptx::mma_commit(bar_empty(s, stage));
+    ptx::mma_commit_pair(bar_empty(s, stage), 0x3);
     if (++stage == NSTAGE) {
       stage = 0;
       phase ^= 1u;
@@ -390,26 +417,29 @@ __device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce,
 }
 
 // ----------------------------------------------------------------------------- MODE_FWD / MODE_DZ loops (static schedule)
+// Pair c of the grid takes units c, c + pairs, c + 2 * pairs, ...
 template <int MODE>
-__device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLayout& s) {
+__device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLayout& s, uint32_t rank) {
   ProducerState ps;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit un = decode_unit<MODE>(p, u);
-    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) ok = produce_tile(p, s, ps, 0, un.m_blk, nb, p.num_k_blocks);
+  for (int u = blockIdx.x >> 1; u < p.num_units && ok; u += gridDim.x >> 1) {
+    const Unit un = decode_unit<MODE>(p, u, rank);
+    for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb)
+      ok = produce_tile(p, s, ps, 0, un.m_blk, nb, p.num_k_blocks, rank);
   }
-  ps.drain(s);
+  ps.drain(s, rank);
 }
 
+// Even CTA only.
 template <int MODE>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, 0, 0);
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN, 0, 0);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit un = decode_unit<MODE>(p, u);
+  for (int u = blockIdx.x >> 1; u < p.num_units && ok; u += gridDim.x >> 1) {
+    const Unit un = decode_unit<MODE>(p, u, 0);
     for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
-      if (!ptx::wait_bounded(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+      if (!ptx::wait_bounded_cluster(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
         abort_cta(p, s);
         ok = false;
         break;
@@ -417,19 +447,26 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, const SmemLayout& 
       ptx::tc_fence_after();
       ok = mma_tile(p, s, tmem_base + acc * BN, p.num_k_blocks, 0, 0, idesc, stage, phase);
       if (!ok) break;
-      ptx::mma_commit(bar_tfull(s, acc));
+      ptx::mma_commit_pair(bar_tfull(s, acc), 0x3);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
   // Wait for every MMA issued so far before TMEM is freed.
-  ptx::mma_commit(bar_drain(s));
+  ptx::mma_commit_pair(bar_drain(s), 0x1);
   ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
+}
+
+// Tells the even CTA that this warp has read its rows of accumulator `acc`.
+__device__ __forceinline__ void release_accumulator(const SmemLayout& s, uint32_t acc, int lane) {
+  ptx::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar_tempty(s, acc), 0));
 }
 
 template <int MODE>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base,
-                                              int warp, int lane) {
+                                              int warp, int lane, uint32_t rank) {
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const int row_in_tile = q * 32 + lane;
   const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -438,8 +475,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
   bool ok = true;
 
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit un = decode_unit<MODE>(p, u);
+  for (int u = blockIdx.x >> 1; u < p.num_units && ok; u += gridDim.x >> 1) {
+    const Unit un = decode_unit<MODE>(p, u, rank);
+    const bool active = un.m_blk * BM < p.rows;       // the odd CTA of a ragged last pair has no rows
     const int t_local = un.m_blk * BM + row_in_tile;  // token within the launch
 
     float m_run = -INFINITY, s_run = 0.0f, zy = 0.0f;
@@ -462,7 +500,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
     }
 
     for (int nb = un.n_lo; nb < un.n_hi; ++nb) {
-      if (!ptx::wait_bounded(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
+      if (!ptx::wait_bounded_cluster(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
         abort_cta(p, s);
         ok = false;
         break;
@@ -470,42 +508,42 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
       ptx::tc_fence_after();
       const uint32_t tcol = lane_addr + acc * BN;
 
-      if constexpr (MODE == MODE_FWD) {
-        const int n0 = nb * BN;
+      if (active) {
+        if constexpr (MODE == MODE_FWD) {
+          const int n0 = nb * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_load32_sync(tcol + c * 32, v);
-          const int col0 = n0 + c * 32;
-          if (col0 + 32 > p.V) {
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_load32_sync(tcol + c * 32, v);
+            const int col0 = n0 + c * 32;
+            if (col0 + 32 > p.V) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j >= p.V) v[j] = -INFINITY;
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= p.V) v[j] = -INFINITY;
+            }
+            const int yo = y - col0;
+            if (static_cast<unsigned>(yo) < 32u) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == yo) zy = v[j];
+              have_zy = true;
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
+            const float m_new = fmaxf(m_run, mx * kLog2e);
+            float acc_s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc_s += ptx::ex2(fmaf(v[j], kLog2e, -m_new));
+            s_run = s_run * ptx::ex2(m_run - m_new) + acc_s;
+            m_run = m_new;
           }
-          const int yo = y - col0;
-          if (static_cast<unsigned>(yo) < 32u) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j == yo) zy = v[j];
-            have_zy = true;
-          }
-          float mx = v[0];
-#pragma unroll
-          for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
-          const float m_new = fmaxf(m_run, mx * kLog2e);
-          float acc_s = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc_s += ptx::ex2(fmaf(v[j], kLog2e, -m_new));
-          s_run = s_run * ptx::ex2(m_run - m_new) + acc_s;
-          m_run = m_new;
+        } else {
+          epi_bf16_tile<true>(&p.tmOut, tcol, nb * BN, un.m_blk * BM + q * 32, staging0, box_count, lane, gt, lse2,
+                              y);
         }
-      } else {
-        epi_bf16_tile<true>(&p.tmOut, tcol, nb * BN, un.m_blk * BM + q * 32, staging0, box_count, lane, gt, lse2, y);
       }
-
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar_tempty(s, acc));
+      release_accumulator(s, acc, lane);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -522,47 +560,66 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
 }
 
 // ----------------------------------------------------------------------------- MODE_DHW loops (dynamic schedule)
-// The producer takes the next tile index from the global counter and passes
-// it to the MMA thread and the epilogue warps through a ring of kTileRing
-// slots in shared memory (tile_full: published; tile_empty: read by all five
-// consumers).  An index >= the tile count ends every role's loop.
-__device__ __forceinline__ void dhw_producer(const GemmParams& p, const SmemLayout& s) {
+// The even CTA's producer takes the next tile index from the global counter,
+// writes it into slot i % kTileRing of both CTAs' rings and arrives on both
+// CTAs' tile_full barriers; the consumers (the even CTA's MMA thread, the odd
+// CTA's producer and all eight epilogue warps) read their own ring and arrive
+// on the even CTA's tile_empty barrier.  An index >= the tile count ends every
+// role's loop.
+__device__ __forceinline__ uint32_t ring_addr(const SmemLayout& s, int slot) {
+  return ptx::smem_u32(const_cast<int*>(s.tile_ring + slot));
+}
+
+__device__ __forceinline__ void dhw_producer(const GemmParams& p, const SmemLayout& s, uint32_t rank) {
   ProducerState ps;
   const int total = p.n_dh_tiles + p.n_dw_tiles;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
     const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
-    if (!ptx::wait_bounded(bar_tile_empty(s, slot), ph ^ 1u, p.timeout_ns, s.abort_flag)) {
-      abort_cta(p, s);
-      break;
+    int t;
+    if (rank == 0) {
+      if (!ptx::wait_bounded_cluster(bar_tile_empty(s, slot), ph ^ 1u, p.timeout_ns, s.abort_flag)) {
+        abort_cta(p, s);
+        break;
+      }
+      t = atomicAdd(p.tile_counter, 1);
+      s.tile_ring[slot] = t;
+      ptx::st_shared_cluster_u32(ptx::mapa(ring_addr(s, slot), 1), static_cast<uint32_t>(t));
+      ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_full(s, slot), 0));
+      ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_full(s, slot), 1));
+    } else {
+      if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
+        abort_cta(p, s);
+        break;
+      }
+      t = s.tile_ring[slot];
+      ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     }
-    const int t = atomicAdd(p.tile_counter, 1);
-    s.tile_ring[slot] = t;
-    ptx::mbar_arrive(bar_tile_full(s, slot));
     if (t >= total) break;
-    const Tile ti = decode_dhw(p, t);
-    if (!produce_tile(p, s, ps, 1 + ti.family, ti.m_blk, ti.nb, ti.num_k)) break;
+    const Tile ti = decode_dhw(p, t, rank);
+    if (!produce_tile(p, s, ps, 1 + ti.family, ti.m_blk, ti.nb, ti.num_k, rank)) break;
   }
-  ps.drain(s);
+  ps.drain(s, rank);
 }
 
+// Even CTA only.
 __device__ __forceinline__ void dhw_mma(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
-  constexpr uint32_t idesc_dh = ptx::idesc_bf16_f32(BM, BN, 0, 1);
-  constexpr uint32_t idesc_dw = ptx::idesc_bf16_f32(BM, BN, 1, 1);
+  constexpr uint32_t idesc_dh = ptx::idesc_bf16_f32(2 * BM, BN, 0, 1);
+  constexpr uint32_t idesc_dw = ptx::idesc_bf16_f32(2 * BM, BN, 1, 1);
   const int total = p.n_dh_tiles + p.n_dw_tiles;
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
     const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
-    if (!ptx::wait_bounded(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
+    if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       break;
     }
     const int t = s.tile_ring[slot];
-    ptx::mbar_arrive(bar_tile_empty(s, slot));
+    ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     if (t >= total) break;
-    const Tile ti = decode_dhw(p, t);
-    if (!ptx::wait_bounded(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+    const Tile ti = decode_dhw(p, t, 0);
+    if (!ptx::wait_bounded_cluster(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       break;
     }
@@ -570,16 +627,16 @@ __device__ __forceinline__ void dhw_mma(const GemmParams& p, const SmemLayout& s
     if (!mma_tile(p, s, tmem_base + acc * BN, ti.num_k, static_cast<uint32_t>(ti.family), 1u,
                   ti.family ? idesc_dw : idesc_dh, stage, phase))
       break;
-    ptx::mma_commit(bar_tfull(s, acc));
+    ptx::mma_commit_pair(bar_tfull(s, acc), 0x3);
     acc ^= 1u;
     if (acc == 0) acc_phase ^= 1u;
   }
-  ptx::mma_commit(bar_drain(s));
+  ptx::mma_commit_pair(bar_drain(s), 0x1);
   ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
 }
 
 __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base, int warp,
-                                             int lane) {
+                                             int lane, uint32_t rank) {
   const int q = warp & 3;
   const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
@@ -588,30 +645,31 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayo
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
     const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
-    if (!ptx::wait_bounded(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
+    if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       break;
     }
     const int t = s.tile_ring[slot];
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar_tile_empty(s, slot));
+    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     if (t >= total) break;
-    const Tile ti = decode_dhw(p, t);
-    if (!ptx::wait_bounded(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
+    const Tile ti = decode_dhw(p, t, rank);
+    if (!ptx::wait_bounded_cluster(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       break;
     }
     ptx::tc_fence_after();
     const uint32_t tcol = lane_addr + acc * BN;
-    if (ti.family == 0)
-      epi_bf16_tile<false>(&p.tmOut, tcol, ti.nb * BN, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count, lane,
-                           0.0f, 0.0f, -1);
-    else
-      epi_f32_tile(&p.tmOut2, p.reduce_out != 0, tcol, ti.nb * BN, ti.m_blk * BM + q * 32, staging0, box_count,
-                   lane);
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar_tempty(s, acc));
+    if (ti.family == 0) {
+      if (ti.m_blk * BM < p.rows)
+        epi_bf16_tile<false>(&p.tmOut, tcol, ti.nb * BN, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count,
+                             lane, 0.0f, 0.0f, -1);
+    } else {
+      if (ti.m_blk * BM < p.V)
+        epi_f32_tile(&p.tmOut2, p.reduce_out != 0, tcol, ti.nb * BN, ti.m_blk * BM + q * 32, staging0, box_count,
+                     lane);
+    }
+    release_accumulator(s, acc, lane);
     acc ^= 1u;
     if (acc == 0) acc_phase ^= 1u;
   }
@@ -621,11 +679,13 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayo
 
 // ----------------------------------------------------------------------------- the GEMM kernel
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const SmemLayout s = carve_smem<MODE>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
@@ -634,12 +694,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar_tfull(s, i), 1);
-      ptx::mbar_init(bar_tempty(s, i), kEpiWarps);
+      ptx::mbar_init(bar_tempty(s, i), 2 * kEpiWarps);
     }
     ptx::mbar_init(bar_drain(s), 1);
     for (int i = 0; i < kTileRing; ++i) {
       ptx::mbar_init(bar_tile_full(s, i), 1);
-      ptx::mbar_init(bar_tile_empty(s, i), 1 + kEpiWarps);
+      ptx::mbar_init(bar_tile_empty(s, i), 2 + 2 * kEpiWarps);
     }
     *s.abort_flag = 0;
     ptx::fence_barrier_init();
@@ -656,24 +716,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), TMEM_COLS);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(ptx::smem_u32(s.tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
   }
+  // Both CTAs' barriers are initialised and their TMEM allocated before any
+  // cross-CTA signal.
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
 
   if (warp == 0) {
     if (ptx::elect_one()) {
       if constexpr (MODE == MODE_DHW)
-        dhw_producer(p, s);
+        dhw_producer(p, s, rank);
       else
-        producer_loop<MODE>(p, s);
+        producer_loop<MODE>(p, s, rank);
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (ptx::elect_one()) {
+    if (rank == 0 && ptx::elect_one()) {
       if constexpr (MODE == MODE_DHW)
         dhw_mma(p, s, tmem_base);
       else
@@ -682,16 +744,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncwarp();
   } else {
     if constexpr (MODE == MODE_DHW)
-      dhw_epilogue(p, s, tmem_base, warp, lane);
+      dhw_epilogue(p, s, tmem_base, warp, lane, rank);
     else
-      epilogue_loop<MODE>(p, s, tmem_base, warp, lane);
+      epilogue_loop<MODE>(p, s, tmem_base, warp, lane, rank);
   }
 
+  // No CTA leaves while its peer may still signal its barriers or use the
+  // pair's TMEM.
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
