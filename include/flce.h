@@ -152,6 +152,52 @@ FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const in
                                           float* loss, float* lse, float* logp, int64_t* n_valid,
                                           int32_t* device_status, void* stream);
 
+/* ---- vocab-parallel split ---------------------------------------------------
+ * The vocabulary split into shards of consecutive rows, as when the LM head is
+ * tensor-parallel over the vocab ("让长序列 MoE RL 训练更好调：Megatron-Lite /
+ * bumblebee 的优化实践", section 2.3 Step 1: a 248,320-row vocab over two ranks
+ * gives 124,160 columns per rank).  Each shard reduces its own logit columns to
+ * a per-row log-sum-exp; the shards' partials combine exactly as the vocab
+ * ranges inside one flce_forward call do (running max / log-sum-exp merge), so
+ * the combined results equal flce_forward on the whole vocabulary.  Moving the
+ * partials between ranks (an all-gather of 2 floats per token) and summing the
+ * dH partials (an all-reduce) are the caller's collectives.
+ *
+ * Forward of one shard: W_shard [V_shard, Hd] holds global vocab rows
+ * [vocab_offset, vocab_offset + V_shard) of a V_total vocabulary.
+ *   shard_lse [T] fp32   log sum_{v in shard} exp(z_{t,v})
+ *   shard_zy  [T] fp32   z_{t,y_t} when y_t lies in the shard, else 0
+ *   workspace            >= flce_forward_workspace_size(T, Hd, V_shard)
+ * ignore_index must lie outside [0, V_total). */
+FLCE_API flce_status flce_forward_shard(const void* H, const void* W_shard, const int64_t* targets, int64_t T,
+                                        int64_t Hd, int64_t V_shard, int64_t vocab_offset, int64_t V_total,
+                                        int64_t ignore_index, float* shard_lse, float* shard_zy, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace flce_combine_shards() needs (0 if n_shards is outside [1, 64]). */
+FLCE_API size_t flce_combine_workspace_size(int64_t T, int32_t n_shards);
+
+/* Combine the partials of n_shards shards (1..64), merged in shard order:
+ *   shard_lse, shard_zy  [n_shards, T] fp32 (shard r's rows at offset r*T)
+ * Outputs and reductions as flce_forward over the V_total vocabulary; targets
+ * outside [0, V_total) that are not ignore_index set FLCE_ERR_TARGET_RANGE in
+ * the workspace status word. */
+FLCE_API flce_status flce_combine_shards(const float* shard_lse, const float* shard_zy, int32_t n_shards,
+                                         const int64_t* targets, int64_t T, int64_t V_total, int64_t ignore_index,
+                                         int32_t reduction, float* loss, float* lse, float* logp, int64_t* n_valid,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of one shard, given the combined lse [T]: dW_shard [V_shard, Hd]
+ * fp32 is this shard's rows of dW; dH_partial [T, Hd] bf16 is this shard's
+ * term sum_{v in shard} dZ_{t,v} w_v of dH (the shards' partials sum to dH).
+ * g_t counts valid rows against the whole vocabulary.  Workspace as
+ * flce_backward_workspace_size(T, Hd, V_shard). */
+FLCE_API flce_status flce_backward_shard(const float* dloss, const void* H, const void* W_shard,
+                                         const int64_t* targets, const float* lse, int64_t T, int64_t Hd,
+                                         int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t ignore_index,
+                                         int32_t reduction, void* dH_partial, float* dW_shard, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* Synchronizes `stream`, then reads the device status word of the latest call
  * made with `workspace` into *out (an flce_status value). */
 FLCE_API flce_status flce_read_device_status(const void* workspace, void* stream, int32_t* out);

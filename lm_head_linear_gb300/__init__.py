@@ -13,8 +13,11 @@ from .binding import (  # noqa: F401
     SIGNATURES,
     flce_backward,
     flce_backward_chunk_tokens,
+    flce_backward_shard,
+    flce_combine_shards,
     flce_backward_workspace_size,
     flce_forward,
+    flce_forward_shard,
     flce_forward_workspace_size,
     flce_profile_collect,
     flce_profile_enable,

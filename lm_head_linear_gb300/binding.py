@@ -33,6 +33,12 @@ SIGNATURES = {
     "flce_backward_chunk_tokens": (_I64, [_I64, _I64, _I64, ctypes.c_size_t]),
     "flce_forward": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P]),
+    "flce_forward_shard": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_combine_workspace_size": (ctypes.c_size_t, [_I64, _I32]),
+    "flce_combine_shards": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                   _P]),
+    "flce_backward_shard": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32, _P, _P, _P,
+                                   ctypes.c_size_t, _P]),
     "flce_backward": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "flce_status_string": (ctypes.c_char_p, [_I32]),
@@ -193,6 +199,68 @@ def flce_backward(dloss: torch.Tensor, H: torch.Tensor, W: torch.Tensor, targets
     st = lib.flce_backward(_ptr(dloss), _ptr(H), _ptr(W), _ptr(targets), _ptr(lse), T, Hd, V, int(ignore_index),
                            red, _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream_handle(stream))
     _check(st)
+    return dH, dW, ws
+
+
+def flce_forward_shard(H: torch.Tensor, W_shard: torch.Tensor, targets: torch.Tensor, vocab_offset: int,
+                       V_total: int, ignore_index: int = -100, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Run ``flce_forward_shard``; returns ``(shard_lse [T], shard_zy [T], workspace)``."""
+    _check_inputs(H, W_shard, targets)
+    lib = load_library()
+    T, Hd = H.shape
+    Vs = W_shard.shape[0]
+    dev = H.device
+    shard_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    shard_zy = torch.empty(T, dtype=torch.float32, device=dev)
+    ws = _workspace(lib.flce_forward_workspace_size(T, Hd, Vs), dev, workspace)
+    _check(lib.flce_forward_shard(_ptr(H), _ptr(W_shard), _ptr(targets), T, Hd, Vs, int(vocab_offset), int(V_total),
+                                  int(ignore_index), _ptr(shard_lse), _ptr(shard_zy), _ptr(ws), ws.numel(),
+                                  _stream_handle(stream)))
+    return shard_lse, shard_zy, ws
+
+
+def flce_combine_shards(shard_lse: torch.Tensor, shard_zy: torch.Tensor, targets: torch.Tensor, V_total: int,
+                        ignore_index: int = -100, reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
+                        stream=None):
+    """Run ``flce_combine_shards`` on [n_shards, T] partials; returns ``(loss, lse, logp, n_valid, workspace)``."""
+    lib = load_library()
+    n_shards, T = shard_lse.shape
+    if shard_zy.shape != shard_lse.shape or targets.shape != (T,):
+        raise ValueError("shard_lse, shard_zy [n_shards, T] and targets [T]")
+    shard_lse = shard_lse.contiguous()
+    shard_zy = shard_zy.contiguous()
+    red = REDUCTIONS[reduction]
+    dev = shard_lse.device
+    loss = torch.empty(T if red == 0 else 1, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    ws = _workspace(lib.flce_combine_workspace_size(T, n_shards), dev, workspace)
+    _check(lib.flce_combine_shards(_ptr(shard_lse), _ptr(shard_zy), n_shards, _ptr(targets), T, int(V_total),
+                                   int(ignore_index), red, _ptr(loss), _ptr(lse), _ptr(logp), _ptr(n_valid),
+                                   _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return loss, lse, logp, n_valid, ws
+
+
+def flce_backward_shard(dloss: torch.Tensor, H: torch.Tensor, W_shard: torch.Tensor, targets: torch.Tensor,
+                        lse: torch.Tensor, vocab_offset: int, V_total: int, ignore_index: int = -100,
+                        reduction: str = "mean", workspace: Optional[torch.Tensor] = None, stream=None):
+    """Run ``flce_backward_shard``; returns ``(dH_partial bf16 [T, Hd], dW_shard fp32 [V_shard, Hd], workspace)``."""
+    _check_inputs(H, W_shard, targets)
+    lib = load_library()
+    T, Hd = H.shape
+    Vs = W_shard.shape[0]
+    red = REDUCTIONS[reduction]
+    dev = H.device
+    dloss = dloss.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
+    if dloss.numel() != (T if red == 0 else 1):
+        raise ValueError("dloss must have one element (mean / sum) or T elements (none)")
+    dH = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((Vs, Hd), dtype=torch.float32, device=dev)
+    ws = _workspace(lib.flce_backward_workspace_size(T, Hd, Vs), dev, workspace)
+    _check(lib.flce_backward_shard(_ptr(dloss), _ptr(H), _ptr(W_shard), _ptr(targets), _ptr(lse.contiguous()), T, Hd,
+                                   Vs, int(vocab_offset), int(V_total), int(ignore_index), red, _ptr(dH), _ptr(dW),
+                                   _ptr(ws), ws.numel(), _stream_handle(stream)))
     return dH, dW, ws
 
 

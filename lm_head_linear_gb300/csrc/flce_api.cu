@@ -37,6 +37,7 @@ flce_status fail(flce_status st, const char* fmt, ...) {
 constexpr size_t kHeaderBytes = 256;  // status word and spare scalars at the start of each workspace
 constexpr int kMaxSplit = 16;         // forward: vocab ranges per token block
 constexpr int64_t kDefaultChunk = 8192;
+constexpr int32_t kMaxShards = 64;    // vocab shards one combine call merges
 
 uint64_t g_timeout_ns = 4000000000ull;
 
@@ -305,6 +306,219 @@ flce_status static_scratch_address(void** out) {
   return FLCE_OK;
 }
 
+// ------------------------------------------------------------------ shared launch sequences
+// Logit tiles of H against W rows [0, V) (global ids vocab_offset + row): per
+// row and vocab range, the running max / sum-exp partials and the target
+// logit (when these rows own the target) go to the workspace layout L.
+flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, const void* W, const int64_t* targets,
+                              int64_t T, int64_t Hd, int64_t V, int64_t vocab_offset, int64_t ignore_index,
+                              uint8_t* ws, FwdLayout* L_out) {
+  flce_status st;
+  const int64_t m_pairs = cdiv(T, 2 * BM);
+  const int64_t n_blocks = cdiv(V, BN);
+  const int n_split = pick_split(m_pairs, n_blocks, dev->pairs[MODE_FWD]);
+  const FwdLayout L = fwd_layout(T, n_split);
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = make_map(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
+  if ((st = make_map(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
+  p.num_m_pairs = static_cast<int32_t>(m_pairs);
+  p.num_n_blocks = static_cast<int32_t>(n_blocks);
+  p.num_k_blocks = static_cast<int32_t>(Hd / BK);
+  p.n_split = n_split;
+  p.num_units = static_cast<int32_t>(m_pairs * n_split);
+  p.row0 = 0;
+  p.rows = static_cast<int32_t>(T);
+  p.T = static_cast<int32_t>(T);
+  p.V = static_cast<int32_t>(V);
+  p.part_stride = static_cast<int32_t>(L.part_stride);
+  p.vocab_offset = vocab_offset;
+  p.ignore_index = ignore_index;
+  p.targets = targets;
+  p.partials = reinterpret_cast<float2*>(ws + L.partials_off);
+  p.zy = reinterpret_cast<float*>(ws + L.zy_off);
+  p.status = reinterpret_cast<int32_t*>(ws);
+  p.timeout_ns = g_timeout_ns;
+  const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_FWD], p.num_units));
+  KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, 2.0 * T * Hd * V,
+                 2.0 * (T * Hd + V * Hd) + 8.0 * n_split * T + 4.0 * T);
+  gemm_kernel<MODE_FWD><<<grid, kThreads, smem_bytes_for(MODE_FWD), s>>>(p);
+  ks.done();
+  if ((st = check_launch("fwd_logits_lse")) != FLCE_OK) return st;
+  *L_out = L;
+  return FLCE_OK;
+}
+
+// Partials of layout L (n_split ranges, z_y) -> lse, logp, loss, n_valid.
+flce_status launch_finalize_reduce(cudaStream_t s, uint8_t* ws, const FwdLayout& L, const int64_t* targets, int64_t T,
+                                   int64_t V_total, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
+                                   float* logp, int64_t* n_valid) {
+  flce_status st;
+  FinalizeParams f;
+  f.partials = reinterpret_cast<const float2*>(ws + L.partials_off);
+  f.zy = reinterpret_cast<const float*>(ws + L.zy_off);
+  f.targets = targets;
+  f.lse = lse;
+  f.logp = logp;
+  f.loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
+  f.block_sum = reinterpret_cast<double*>(ws + L.bsum_off);
+  f.block_count = reinterpret_cast<int64_t*>(ws + L.bcnt_off);
+  f.status = reinterpret_cast<int32_t*>(ws);
+  f.ignore_index = ignore_index;
+  f.T = static_cast<int32_t>(T);
+  f.V = static_cast<int32_t>(V_total);
+  f.n_split = L.n_split;
+  f.part_stride = static_cast<int32_t>(L.part_stride);
+  {
+    KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (8.0 * L.n_split + 4 + 8 + 12) * T);
+    fwd_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(f);
+    ks.done();
+    if ((st = check_launch("fwd_finalize")) != FLCE_OK) return st;
+  }
+  {
+    KernelScope ks(FLCE_KERNEL_FWD_REDUCE, s, 0.0, 16.0 * L.num_fin_blocks);
+    fwd_reduce_kernel<<<1, kReduceThreads, 0, s>>>(f.block_sum, f.block_count, L.num_fin_blocks, reduction, loss,
+                                                   n_valid);
+    ks.done();
+    if ((st = check_launch("fwd_reduce")) != FLCE_OK) return st;
+  }
+  return FLCE_OK;
+}
+
+flce_status check_shard(int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t ignore_index) {
+  if (V_total < 1 || V_total >= (int64_t(1) << 31))
+    return fail(FLCE_ERR_INVALID_ARG, "V_total = %lld out of range", (long long)V_total);
+  if (V_shard < 1 || vocab_offset < 0 || vocab_offset + V_shard > V_total)
+    return fail(FLCE_ERR_INVALID_ARG, "shard [%lld, %lld) does not lie inside [0, V_total = %lld)",
+                (long long)vocab_offset, (long long)(vocab_offset + V_shard), (long long)V_total);
+  if (ignore_index >= 0 && ignore_index < V_total)
+    return fail(FLCE_ERR_INVALID_ARG, "ignore_index %lld lies inside [0, V_total)", (long long)ignore_index);
+  return FLCE_OK;
+}
+
+// The backward over W rows [0, V) with global ids vocab_offset + row; g_t is
+// computed against the full vocabulary [0, V_total).
+flce_status backward_impl(const float* dloss, const void* H, const void* W, const int64_t* targets, const float* lse,
+                          int64_t T, int64_t Hd, int64_t V, int64_t vocab_offset, int64_t V_total,
+                          int64_t ignore_index, int32_t reduction, void* dH, float* dW, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  flce_status st;
+  if (!dW || (T > 0 && (!dloss || !lse || !dH))) return fail(FLCE_ERR_INVALID_ARG, "dloss, lse, dH or dW is NULL");
+  if ((reinterpret_cast<uintptr_t>(dH) | reinterpret_cast<uintptr_t>(dW)) & 15)
+    return fail(FLCE_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const int64_t chunk = flce_backward_chunk_tokens(T, Hd, V, workspace_bytes);
+  if (chunk <= 0)
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes is too small (need %zu)", workspace_bytes,
+                flce_backward_workspace_size(T, Hd, V));
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+
+  if (T == 0) {
+    CUDA_TRY(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * Hd, s));
+    return FLCE_OK;
+  }
+  const BwdLayout L = bwd_layout(T, V, chunk);
+  float* g = reinterpret_cast<float*>(ws + L.g_off);
+  void* dz = ws + L.dz_off;
+
+  {
+    KernelScope ks(FLCE_KERNEL_BWD_PREP, s, 0.0, 12.0 * T);
+    bwd_prep_kernel<<<1, kReduceThreads, 0, s>>>(dloss, targets, static_cast<int>(T), static_cast<int>(V_total),
+                                                 ignore_index, reduction, g, status);
+    ks.done();
+    if ((st = check_launch("bwd_prep")) != FLCE_OK) return st;
+  }
+  const int64_t n_hd_blocks = cdiv(Hd, BN);
+  CUtensorMap tm_H_k, tm_W_k, tm_W_mn, tm_H_mn, tm_dH, tm_dW_out;
+  if ((st = make_map(&tm_H_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_W_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, 64, 64)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_H_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, 64, 64)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_dH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dH, Hd, T, Hd * 2, 64, 32)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
+
+  const int64_t n_chunks = cdiv(T, chunk);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + L.cnt_off);
+  CUDA_TRY(cudaMemsetAsync(counters, 0, sizeof(int32_t) * static_cast<size_t>(n_chunks), s));
+
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int64_t c0 = c * chunk;
+    const int64_t rows = std::min<int64_t>(chunk, T - c0);
+    const int64_t m_pairs = cdiv(rows, 2 * BM);
+    CUtensorMap tm_dz_store, tm_dz_k, tm_dz_mn;
+    if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 32)) != FLCE_OK)
+      return st;
+    if ((st = make_map(&tm_dz_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, BK, BM)) != FLCE_OK)
+      return st;
+    if ((st = make_map(&tm_dz_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 64)) != FLCE_OK)
+      return st;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.row0 = static_cast<int32_t>(c0);
+    p.rows = static_cast<int32_t>(rows);
+    p.T = static_cast<int32_t>(T);
+    p.V = static_cast<int32_t>(V);
+    p.vocab_offset = vocab_offset;
+    p.ignore_index = ignore_index;
+    p.targets = targets;
+    p.lse = lse;
+    p.g = g;
+    p.status = status;
+    p.timeout_ns = g_timeout_ns;
+    p.n_split = 1;
+
+    // (1) recomputed logit tiles -> dZ chunk
+    p.tmA = tm_H_k;
+    p.tmB = tm_W_k;
+    p.tmOut = tm_dz_store;
+    p.num_m_pairs = static_cast<int32_t>(m_pairs);
+    p.num_n_blocks = static_cast<int32_t>(cdiv(V, BN));
+    p.num_k_blocks = static_cast<int32_t>(Hd / BK);
+    p.num_units = p.num_m_pairs * p.num_n_blocks;
+    {
+      const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DZ], p.num_units));
+      KernelScope ks(FLCE_KERNEL_BWD_DZ, s, 2.0 * rows * Hd * V,
+                     2.0 * (rows * Hd + V * Hd) + 2.0 * rows * V + 16.0 * rows);
+      gemm_kernel<MODE_DZ><<<grid, kThreads, smem_bytes_for(MODE_DZ), s>>>(p);
+      ks.done();
+      if ((st = check_launch("bwd_dz")) != FLCE_OK) return st;
+    }
+    // (2) dH rows of the chunk = dZ W and dW (+)= dZ^T H[chunk] in one launch;
+    //     the first chunk stores dW, later chunks add to it, in chunk order.
+    p.tmA = tm_dz_k;
+    p.tmB = tm_W_mn;
+    p.tmOut = tm_dH;
+    p.tmA2 = tm_dz_mn;
+    p.tmB2 = tm_H_mn;
+    p.tmOut2 = tm_dW_out;
+    p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
+    p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
+    p.num_k_blocks2 = static_cast<int32_t>(cdiv(rows, BK));
+    p.n_dh_tiles = static_cast<int32_t>(m_pairs * n_hd_blocks);
+    p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
+    p.reduce_out = c > 0 ? 1 : 0;
+    p.tile_counter = counters + c;
+    {
+      const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DHW], p.n_dh_tiles + p.n_dw_tiles));
+      KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 4.0 * rows * Hd * V,
+                     4.0 * rows * V + 2.0 * V * Hd + 4.0 * rows * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd);
+      gemm_kernel<MODE_DHW><<<grid, kThreads, smem_bytes_for(MODE_DHW), s>>>(p);
+      ks.done();
+      if ((st = check_launch("bwd_dh_dw")) != FLCE_OK) return st;
+    }
+  }
+  return FLCE_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -431,7 +645,6 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
   if ((st = get_encoder()) != FLCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* status = reinterpret_cast<int32_t*>(ws);
   CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
 
   if (T == 0) {
@@ -439,71 +652,89 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
     if (n_valid) CUDA_TRY(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
     return FLCE_OK;
   }
+  FwdLayout L;
+  if ((st = launch_logits_lse(dev, s, H, W, targets, T, Hd, V, 0, ignore_index, ws, &L)) != FLCE_OK) return st;
+  return launch_finalize_reduce(s, ws, L, targets, T, V, ignore_index, reduction, loss, lse, logp, n_valid);
+}
 
-  const int64_t m_pairs = cdiv(T, 2 * BM);
-  const int64_t n_blocks = cdiv(V, BN);
-  const int n_split = pick_split(m_pairs, n_blocks, dev->pairs[MODE_FWD]);
-  const FwdLayout L = fwd_layout(T, n_split);
+size_t flce_combine_workspace_size(int64_t T, int32_t n_shards) {
+  if (T < 0 || n_shards < 1 || n_shards > kMaxShards) return 0;
+  return fwd_layout(T, n_shards).total;
+}
 
-  GemmParams p;
-  std::memset(&p, 0, sizeof(p));
-  if ((st = make_map(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
-  if ((st = make_map(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
-  p.num_m_pairs = static_cast<int32_t>(m_pairs);
-  p.num_n_blocks = static_cast<int32_t>(n_blocks);
-  p.num_k_blocks = static_cast<int32_t>(Hd / BK);
-  p.n_split = n_split;
-  p.num_units = static_cast<int32_t>(m_pairs * n_split);
-  p.row0 = 0;
-  p.rows = static_cast<int32_t>(T);
-  p.T = static_cast<int32_t>(T);
-  p.V = static_cast<int32_t>(V);
-  p.part_stride = static_cast<int32_t>(L.part_stride);
-  p.ignore_index = ignore_index;
-  p.targets = targets;
-  p.partials = reinterpret_cast<float2*>(ws + L.partials_off);
-  p.zy = reinterpret_cast<float*>(ws + L.zy_off);
-  p.status = status;
-  p.timeout_ns = g_timeout_ns;
+flce_status flce_forward_shard(const void* H, const void* W_shard, const int64_t* targets, int64_t T, int64_t Hd,
+                               int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t ignore_index,
+                               float* shard_lse, float* shard_zy, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  flce_status st = check_shard(V_shard, vocab_offset, V_total, ignore_index);
+  if (st != FLCE_OK) return st;
+  if ((st = check_common(H, W_shard, targets, T, Hd, V_shard, -1, FLCE_REDUCTION_SUM)) != FLCE_OK) return st;
+  if (T > 0 && (!shard_lse || !shard_zy)) return fail(FLCE_ERR_INVALID_ARG, "shard_lse or shard_zy is NULL");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (workspace_bytes < flce_forward_workspace_size(T, Hd, V_shard))
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
+                flce_forward_workspace_size(T, Hd, V_shard));
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  if (T == 0) return FLCE_OK;
+  FwdLayout L;
+  if ((st = launch_logits_lse(dev, s, H, W_shard, targets, T, Hd, V_shard, vocab_offset, ignore_index, ws, &L)) !=
+      FLCE_OK)
+    return st;
+  KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (8.0 * L.n_split + 4 + 8 + 8) * T);
+  fwd_shard_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(
+      reinterpret_cast<const float2*>(ws + L.partials_off), reinterpret_cast<const float*>(ws + L.zy_off), targets,
+      static_cast<int>(T), vocab_offset, static_cast<int>(V_shard), L.n_split, static_cast<int>(L.part_stride),
+      shard_lse, shard_zy);
+  ks.done();
+  return check_launch("fwd_shard_finalize");
+}
 
-  const double mma_flops = 2.0 * T * Hd * V;
-  const double in_bytes = 2.0 * (T * Hd + V * Hd);
-  {
-    const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_FWD], p.num_units));
-    KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, mma_flops, in_bytes + 8.0 * n_split * T + 4.0 * T);
-    gemm_kernel<MODE_FWD><<<grid, kThreads, smem_bytes_for(MODE_FWD), s>>>(p);
-    ks.done();
-    if ((st = check_launch("fwd_logits_lse")) != FLCE_OK) return st;
+flce_status flce_combine_shards(const float* shard_lse, const float* shard_zy, int32_t n_shards,
+                                const int64_t* targets, int64_t T, int64_t V_total, int64_t ignore_index,
+                                int32_t reduction, float* loss, float* lse, float* logp, int64_t* n_valid,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_shards < 1 || n_shards > kMaxShards)
+    return fail(FLCE_ERR_INVALID_ARG, "n_shards = %d outside [1, %d]", n_shards, kMaxShards);
+  if (T < 0 || T >= (int64_t(1) << 31)) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
+  if (V_total < 1 || V_total >= (int64_t(1) << 31))
+    return fail(FLCE_ERR_INVALID_ARG, "V_total = %lld out of range", (long long)V_total);
+  if (reduction < 0 || reduction > 2) return fail(FLCE_ERR_INVALID_ARG, "unknown reduction %d", reduction);
+  if (ignore_index >= 0 && ignore_index < V_total)
+    return fail(FLCE_ERR_INVALID_ARG, "ignore_index %lld lies inside [0, V_total)", (long long)ignore_index);
+  if (!loss || (T > 0 && (!shard_lse || !shard_zy || !targets || !lse || !logp)))
+    return fail(FLCE_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (workspace_bytes < flce_combine_workspace_size(T, n_shards))
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
+                flce_combine_workspace_size(T, n_shards));
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  if (T == 0) {
+    if (reduction != FLCE_REDUCTION_NONE) CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    if (n_valid) CUDA_TRY(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
+    return FLCE_OK;
   }
-  FinalizeParams f;
-  f.partials = p.partials;
-  f.zy = p.zy;
-  f.targets = targets;
-  f.lse = lse;
-  f.logp = logp;
-  f.loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
-  f.block_sum = reinterpret_cast<double*>(ws + L.bsum_off);
-  f.block_count = reinterpret_cast<int64_t*>(ws + L.bcnt_off);
-  f.status = status;
-  f.ignore_index = ignore_index;
-  f.T = static_cast<int32_t>(T);
-  f.V = static_cast<int32_t>(V);
-  f.n_split = n_split;
-  f.part_stride = static_cast<int32_t>(L.part_stride);
+  const FwdLayout L = fwd_layout(T, n_shards);
   {
-    KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (8.0 * n_split + 4 + 8 + 12) * T);
-    fwd_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(f);
+    KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (8.0 * n_shards + 12.0 * n_shards + 4) * T);
+    combine_shards_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(
+        shard_lse, shard_zy, n_shards, static_cast<int>(T), reinterpret_cast<float2*>(ws + L.partials_off),
+        static_cast<int>(L.part_stride), reinterpret_cast<float*>(ws + L.zy_off));
     ks.done();
-    if ((st = check_launch("fwd_finalize")) != FLCE_OK) return st;
+    flce_status st = check_launch("combine_shards");
+    if (st != FLCE_OK) return st;
   }
-  {
-    KernelScope ks(FLCE_KERNEL_FWD_REDUCE, s, 0.0, 16.0 * L.num_fin_blocks);
-    fwd_reduce_kernel<<<1, kReduceThreads, 0, s>>>(f.block_sum, f.block_count, L.num_fin_blocks, reduction, loss,
-                                                   n_valid);
-    ks.done();
-    if ((st = check_launch("fwd_reduce")) != FLCE_OK) return st;
-  }
-  return FLCE_OK;
+  return launch_finalize_reduce(s, ws, L, targets, T, V_total, ignore_index, reduction, loss, lse, logp, n_valid);
 }
 
 flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd,
@@ -532,120 +763,19 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
                           float* dW, void* workspace, size_t workspace_bytes, void* stream) {
   flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
   if (st != FLCE_OK) return st;
-  if (!dW || (T > 0 && (!dloss || !lse || !dH))) return fail(FLCE_ERR_INVALID_ARG, "dloss, lse, dH or dW is NULL");
-  if ((reinterpret_cast<uintptr_t>(dH) | reinterpret_cast<uintptr_t>(dW)) & 15)
-    return fail(FLCE_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
-  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
-  if (reinterpret_cast<uintptr_t>(workspace) & 255)
-    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-  const int64_t chunk = flce_backward_chunk_tokens(T, Hd, V, workspace_bytes);
-  if (chunk <= 0)
-    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes is too small (need %zu)", workspace_bytes,
-                flce_backward_workspace_size(T, Hd, V));
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != FLCE_OK) return st;
-  if ((st = get_encoder()) != FLCE_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* status = reinterpret_cast<int32_t*>(ws);
-  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  return backward_impl(dloss, H, W, targets, lse, T, Hd, V, 0, V, ignore_index, reduction, dH, dW, workspace,
+                       workspace_bytes, stream);
+}
 
-  if (T == 0) {
-    CUDA_TRY(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * Hd, s));
-    return FLCE_OK;
-  }
-  const BwdLayout L = bwd_layout(T, V, chunk);
-  float* g = reinterpret_cast<float*>(ws + L.g_off);
-  void* dz = ws + L.dz_off;
-
-  {
-    KernelScope ks(FLCE_KERNEL_BWD_PREP, s, 0.0, 12.0 * T);
-    bwd_prep_kernel<<<1, kReduceThreads, 0, s>>>(dloss, targets, static_cast<int>(T), static_cast<int>(V),
-                                                 ignore_index, reduction, g, status);
-    ks.done();
-    if ((st = check_launch("bwd_prep")) != FLCE_OK) return st;
-  }
-
-  const int64_t n_hd_blocks = cdiv(Hd, BN);
-  CUtensorMap tm_H_k, tm_W_k, tm_W_mn, tm_H_mn, tm_dH, tm_dW_out;
-  if ((st = make_map(&tm_H_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_W_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, 64, 64)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_H_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, 64, 64)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_dH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dH, Hd, T, Hd * 2, 64, 32)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
-
-  const int64_t n_chunks = cdiv(T, chunk);
-  int32_t* counters = reinterpret_cast<int32_t*>(ws + L.cnt_off);
-  CUDA_TRY(cudaMemsetAsync(counters, 0, sizeof(int32_t) * static_cast<size_t>(n_chunks), s));
-
-  for (int64_t c = 0; c < n_chunks; ++c) {
-    const int64_t c0 = c * chunk;
-    const int64_t rows = std::min<int64_t>(chunk, T - c0);
-    const int64_t m_pairs = cdiv(rows, 2 * BM);
-    CUtensorMap tm_dz_store, tm_dz_k, tm_dz_mn;
-    if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 32)) != FLCE_OK)
-      return st;
-    if ((st = make_map(&tm_dz_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, BK, BM)) != FLCE_OK)
-      return st;
-    if ((st = make_map(&tm_dz_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 64)) != FLCE_OK)
-      return st;
-
-    GemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.row0 = static_cast<int32_t>(c0);
-    p.rows = static_cast<int32_t>(rows);
-    p.T = static_cast<int32_t>(T);
-    p.V = static_cast<int32_t>(V);
-    p.ignore_index = ignore_index;
-    p.targets = targets;
-    p.lse = lse;
-    p.g = g;
-    p.status = status;
-    p.timeout_ns = g_timeout_ns;
-    p.n_split = 1;
-
-    // (1) recomputed logit tiles -> dZ chunk
-    p.tmA = tm_H_k;
-    p.tmB = tm_W_k;
-    p.tmOut = tm_dz_store;
-    p.num_m_pairs = static_cast<int32_t>(m_pairs);
-    p.num_n_blocks = static_cast<int32_t>(cdiv(V, BN));
-    p.num_k_blocks = static_cast<int32_t>(Hd / BK);
-    p.num_units = p.num_m_pairs * p.num_n_blocks;
-    {
-      const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DZ], p.num_units));
-      KernelScope ks(FLCE_KERNEL_BWD_DZ, s, 2.0 * rows * Hd * V,
-                     2.0 * (rows * Hd + V * Hd) + 2.0 * rows * V + 16.0 * rows);
-      gemm_kernel<MODE_DZ><<<grid, kThreads, smem_bytes_for(MODE_DZ), s>>>(p);
-      ks.done();
-      if ((st = check_launch("bwd_dz")) != FLCE_OK) return st;
-    }
-    // (2) dH rows of the chunk = dZ W and dW (+)= dZ^T H[chunk] in one launch;
-    //     the first chunk stores dW, later chunks add to it, in chunk order.
-    p.tmA = tm_dz_k;
-    p.tmB = tm_W_mn;
-    p.tmOut = tm_dH;
-    p.tmA2 = tm_dz_mn;
-    p.tmB2 = tm_H_mn;
-    p.tmOut2 = tm_dW_out;
-    p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
-    p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
-    p.num_k_blocks2 = static_cast<int32_t>(cdiv(rows, BK));
-    p.n_dh_tiles = static_cast<int32_t>(m_pairs * n_hd_blocks);
-    p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
-    p.reduce_out = c > 0 ? 1 : 0;
-    p.tile_counter = counters + c;
-    {
-      const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DHW], p.n_dh_tiles + p.n_dw_tiles));
-      KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 4.0 * rows * Hd * V,
-                     4.0 * rows * V + 2.0 * V * Hd + 4.0 * rows * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd);
-      gemm_kernel<MODE_DHW><<<grid, kThreads, smem_bytes_for(MODE_DHW), s>>>(p);
-      ks.done();
-      if ((st = check_launch("bwd_dh_dw")) != FLCE_OK) return st;
-    }
-  }
-  return FLCE_OK;
+flce_status flce_backward_shard(const float* dloss, const void* H, const void* W_shard, const int64_t* targets,
+                                const float* lse, int64_t T, int64_t Hd, int64_t V_shard, int64_t vocab_offset,
+                                int64_t V_total, int64_t ignore_index, int32_t reduction, void* dH_partial,
+                                float* dW_shard, void* workspace, size_t workspace_bytes, void* stream) {
+  flce_status st = check_shard(V_shard, vocab_offset, V_total, ignore_index);
+  if (st != FLCE_OK) return st;
+  if ((st = check_common(H, W_shard, targets, T, Hd, V_shard, -1, reduction)) != FLCE_OK) return st;
+  return backward_impl(dloss, H, W_shard, targets, lse, T, Hd, V_shard, vocab_offset, V_total, ignore_index,
+                       reduction, dH_partial, dW_shard, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

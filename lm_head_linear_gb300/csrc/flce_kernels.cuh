@@ -106,6 +106,7 @@ struct GemmParams {
   int32_t n_dh_tiles;    // MODE_DHW: dH tiles come first in the tile order ...
   int32_t n_dw_tiles;    // ... then the dW tiles
   int32_t num_k_blocks2; // MODE_DHW: K blocks of a dW tile (tokens of the chunk / 64)
+  int64_t vocab_offset;  // global id of local vocab row 0 (a vocab shard); 0 for the full vocabulary
   int64_t ignore_index;
   const int64_t* targets;
   const float* lse;      // MODE_DZ
@@ -484,17 +485,18 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
     bool have_zy = false;
     int y = -1;
     float gt = 0.0f, lse2 = 0.0f;
+    // y: the target's local vocab column when this launch's vocab rows own it, else -1
     if constexpr (MODE == MODE_FWD) {
       if (t_local < p.rows) {
-        const int64_t yy = p.targets[t_local];
-        if (yy != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
+        const int64_t yy = p.targets[t_local] - p.vocab_offset;
+        if (p.targets[t_local] != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
       }
     } else {
       if (t_local < p.rows) {
         const int t = p.row0 + t_local;
         gt = p.g[t];
         lse2 = p.lse[t] * kLog2e;
-        const int64_t yy = p.targets[t];
+        const int64_t yy = p.targets[t] - p.vocab_offset;
         if (yy >= 0 && yy < p.V) y = static_cast<int>(yy);
       }
     }
@@ -829,6 +831,44 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(const Fi
     p.block_sum[blockIdx.x] = sh_sum[0];
     p.block_count[blockIdx.x] = sh_cnt[0];
   }
+}
+
+// Vocab shard forward: per row, merge the shard's split partials into the
+// shard's log-sum-exp and report the target logit when the shard owns the target.
+__global__ void __launch_bounds__(kFinalizeThreads) fwd_shard_finalize_kernel(
+    const float2* partials, const float* zy, const int64_t* targets, int T, int64_t vocab_offset, int V_shard,
+    int n_split, int part_stride, float* shard_lse, float* shard_zy) {
+  const int t = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  if (t >= T) return;
+  float M = -INFINITY;
+  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, partials[static_cast<size_t>(sp) * part_stride + t].x);
+  float S = 0.0f;
+  for (int sp = 0; sp < n_split; ++sp) {
+    const float2 pr = partials[static_cast<size_t>(sp) * part_stride + t];
+    S += pr.y * exp2f(pr.x - M);
+  }
+  const int64_t yy = targets[t] - vocab_offset;
+  shard_lse[t] = (M + log2f(S)) * kLn2;
+  shard_zy[t] = (yy >= 0 && yy < V_shard) ? zy[t] : 0.0f;
+}
+
+// Cross-shard combine, step 1: shard r's log-sum-exp becomes the partial
+// (lse_r * log2e, 1) of split r, and the target logits are summed in shard
+// order (only the owning shard reports a non-zero one).  fwd_finalize_kernel
+// then merges the partials exactly as it merges the vocab ranges of one launch.
+__global__ void __launch_bounds__(kFinalizeThreads) combine_shards_kernel(const float* shard_lse,
+                                                                         const float* shard_zy, int n_shards, int T,
+                                                                         float2* partials, int part_stride,
+                                                                         float* zy) {
+  const int t = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  if (t >= T) return;
+  float z = 0.0f;
+  for (int r = 0; r < n_shards; ++r) {
+    partials[static_cast<size_t>(r) * part_stride + t] =
+        make_float2(shard_lse[static_cast<size_t>(r) * T + t] * kLog2e, 1.0f);
+    z += shard_zy[static_cast<size_t>(r) * T + t];
+  }
+  zy[t] = z;
 }
 
 // One block: fixed-order sum of the block partials into the scalar loss and n_valid.

@@ -16,6 +16,7 @@ from .flce_oracle import (  # noqa: F401
     logits,
     naive_logits_bytes,
     sampled_rows,
+    shard_partials,
     upstream_grad,
     valid_mask,
 )

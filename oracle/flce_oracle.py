@@ -208,6 +208,34 @@ def dW_rows(H: np.ndarray, W_rows: np.ndarray, targets: np.ndarray, g: np.ndarra
     return out
 
 
+def shard_partials(H: np.ndarray, W_shard: np.ndarray, targets: np.ndarray, vocab_offset: int,
+                   ignore_index: int = -100, row_block: int = 256):
+    """Per-row partials of one vocab shard: the log-sum-exp over the shard's logit
+    columns, and the target logit where the shard holds the target row (0 elsewhere).
+
+    ``W_shard`` holds global vocab rows [vocab_offset, vocab_offset + V_shard).  The
+    shard's lse is the plain definition restricted to its columns; the whole-vocab
+    lse is the log-sum-exp of the shards' lse (the vocab-parallel split of the
+    Megatron-Lite / bumblebee post, section 2.3 Step 1).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W_shard = np.asarray(W_shard, dtype=np.float64)
+    targets = np.asarray(targets, dtype=np.int64)
+    T, Vs = H.shape[0], W_shard.shape[0]
+    local = targets - vocab_offset
+    owned = (targets != ignore_index) & (local >= 0) & (local < Vs)
+    lse = np.zeros(T)
+    zy = np.zeros(T)
+    for r0 in range(0, T, row_block):
+        r1 = min(T, r0 + row_block)
+        Z = logits(H[r0:r1], W_shard)
+        lse[r0:r1] = _row_lse(Z)
+        rows = np.arange(r1 - r0)
+        o = owned[r0:r1]
+        zy[r0:r1][o] = Z[rows[o], local[r0:r1][o]]
+    return lse, zy
+
+
 def naive_logits_bytes(T: int, V: int, bytes_per_elem: int, copies: int = 1) -> int:
     """Bytes of ``copies`` dense [T x V] logits tensors (section 3 of the page;
     section 2.3 Step 1 of the Megatron-Lite / bumblebee post)."""
@@ -216,6 +244,6 @@ def naive_logits_bytes(T: int, V: int, bytes_per_elem: int, copies: int = 1) -> 
 
 __all__ = [
     "ForwardResult", "backward", "dW_rows", "forward", "logits", "naive_logits_bytes",
-    "sampled_rows", "upstream_grad", "valid_mask", "REDUCTIONS",
+    "sampled_rows", "shard_partials", "upstream_grad", "valid_mask", "REDUCTIONS",
 ]
 

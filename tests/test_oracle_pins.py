@@ -279,11 +279,31 @@ def pin_sampled_paths():
     assert np.allclose(dWr, dW[vr], atol=1e-14)
 
 
+def pin_vocab_shards():
+    """Shard partials over a split of the vocabulary: the log-sum-exp of the shards'
+    lse is the whole-vocab lse, each valid target logit comes from exactly one shard,
+    and the shards' dZ-column blocks give dW (every vocab row lives in one shard)."""
+    H, W, y = _rand_case(16, T=9, Hd=8, V=41, n_ignore=2)
+    cuts = [0, 13, 29, 41]
+    f = fo.forward(H, W, y, IGN, "mean")
+    parts = [fo.shard_partials(H, W[a:b], y, a, IGN) for a, b in zip(cuts[:-1], cuts[1:])]
+    lses = np.stack([q[0] for q in parts])
+    m = lses.max(axis=0)
+    assert np.allclose(m + np.log(np.exp(lses - m).sum(axis=0)), f.lse, rtol=0, atol=1e-13)
+    zy = np.stack([q[1] for q in parts]).sum(axis=0)
+    valid = y != IGN
+    Z = H @ W.T
+    assert np.allclose(zy[valid], Z[np.nonzero(valid)[0], y[valid]], atol=1e-13)
+    assert np.all(zy[~valid] == 0.0)
+    owners = sum(((y >= a) & (y < b) & valid).astype(int) for a, b in zip(cuts[:-1], cuts[1:]))
+    assert np.array_equal(owners, valid.astype(int))
+
+
 PINS = [
     pin_w_zero_closed_form, pin_vocab_of_one, pin_torch_library, pin_finite_differences,
     pin_brute_force_tiny, pin_shift_invariance_and_overflow, pin_gradient_sums_vanish,
     pin_ignored_rows, pin_reductions_agree, pin_permutation_equivariance,
-    pin_pages_memory_arithmetic, pin_sampled_paths,
+    pin_pages_memory_arithmetic, pin_sampled_paths, pin_vocab_shards,
 ]
 
 
