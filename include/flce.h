@@ -152,6 +152,22 @@ FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const in
                                           float* loss, float* lse, float* logp, int64_t* n_valid,
                                           int32_t* device_status, void* stream);
 
+/* Scoring: per-token log p(target) and the greedy token, without a loss.
+ * Serves comparing a trainer's token log-probabilities with a rollout
+ * engine's (the token-level agreement checks of the pages' RL write-ups,
+ * e.g. "Long-Sequence MoE RL Training: From First Principles to MI300X"
+ * section 1: rollout then train).  Same logit tiles and log-sum-exp
+ * recurrence as flce_forward; no reduction.
+ *   logp    [T] fp32         z_{t,y_t} - lse_t; 0 on ignored rows
+ *   lse     [T] fp32 or NULL
+ *   argmax  [T] int64 or NULL  argmax_v z_{t,v} over the fp32-accumulated
+ *                              logits, lowest id on ties
+ *   workspace >= flce_score_workspace_size(T, Hd, V) */
+FLCE_API size_t flce_score_workspace_size(int64_t T, int64_t Hd, int64_t V);
+FLCE_API flce_status flce_score(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
+                                int64_t ignore_index, float* logp, float* lse, int64_t* argmax, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* ---- vocab-parallel split ---------------------------------------------------
  * The vocabulary split into shards of consecutive rows, as when the LM head is
  * tensor-parallel over the vocab ("让长序列 MoE RL 训练更好调：Megatron-Lite /

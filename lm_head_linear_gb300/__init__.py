@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     flce_profile_collect,
     flce_profile_enable,
     flce_read_device_status,
+    flce_score,
     flce_set_wait_timeout_ns,
     library_path,
     linear_cross_entropy,

@@ -33,6 +33,8 @@ SIGNATURES = {
     "flce_backward_chunk_tokens": (_I64, [_I64, _I64, _I64, ctypes.c_size_t]),
     "flce_forward": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P]),
+    "flce_score_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "flce_score": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_shard": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_combine_workspace_size": (ctypes.c_size_t, [_I64, _I32]),
     "flce_combine_shards": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t,
@@ -200,6 +202,23 @@ def flce_backward(dloss: torch.Tensor, H: torch.Tensor, W: torch.Tensor, targets
                            red, _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream_handle(stream))
     _check(st)
     return dH, dW, ws
+
+
+def flce_score(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+               workspace: Optional[torch.Tensor] = None, stream=None):
+    """Run ``flce_score``; returns ``(logp [T] fp32, lse [T] fp32, argmax [T] int64, workspace)``."""
+    _check_inputs(H, W, targets)
+    lib = load_library()
+    T, Hd = H.shape
+    V = W.shape[0]
+    dev = H.device
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    argmax = torch.empty(T, dtype=torch.int64, device=dev)
+    ws = _workspace(lib.flce_score_workspace_size(T, Hd, V), dev, workspace)
+    _check(lib.flce_score(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), _ptr(logp), _ptr(lse),
+                          _ptr(argmax), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return logp, lse, argmax, ws
 
 
 def flce_forward_shard(H: torch.Tensor, W_shard: torch.Tensor, targets: torch.Tensor, vocab_offset: int,

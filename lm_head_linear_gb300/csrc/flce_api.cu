@@ -50,7 +50,7 @@ struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
   bool attrs_set = false;
-  int pairs[3] = {0, 0, 0};  // co-resident CTA pairs (clusters of 2) per GEMM mode
+  int pairs[4] = {0, 0, 0, 0};  // co-resident CTA pairs (clusters of 2) per GEMM mode
 };
 
 template <int MODE>
@@ -88,10 +88,13 @@ flce_status device_info(DeviceInfo** out) {
                                   smem_bytes_for(MODE_DZ)));
     CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_DHW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   smem_bytes_for(MODE_DHW)));
+    CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<MODE_SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_bytes_for(MODE_SCORE)));
     flce_status st;
     if ((st = query_pairs<MODE_FWD>(d)) != FLCE_OK) return st;
     if ((st = query_pairs<MODE_DZ>(d)) != FLCE_OK) return st;
     if ((st = query_pairs<MODE_DHW>(d)) != FLCE_OK) return st;
+    if ((st = query_pairs<MODE_SCORE>(d)) != FLCE_OK) return st;
     d.attrs_set = true;
   }
   *out = &d;
@@ -310,9 +313,12 @@ flce_status static_scratch_address(void** out) {
 // Logit tiles of H against W rows [0, V) (global ids vocab_offset + row): per
 // row and vocab range, the running max / sum-exp partials and the target
 // logit (when these rows own the target) go to the workspace layout L.
+// With `best_val` / `best_idx` set (scoring), the argmax variant also records
+// each row's largest logit and its global id per vocab range.
 flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, const void* W, const int64_t* targets,
                               int64_t T, int64_t Hd, int64_t V, int64_t vocab_offset, int64_t ignore_index,
-                              uint8_t* ws, FwdLayout* L_out) {
+                              uint8_t* ws, FwdLayout* L_out, float* best_val = nullptr,
+                              int32_t* best_idx = nullptr) {
   flce_status st;
   const int64_t m_pairs = cdiv(T, 2 * BM);
   const int64_t n_blocks = cdiv(V, BN);
@@ -337,12 +343,18 @@ flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, co
   p.targets = targets;
   p.partials = reinterpret_cast<float2*>(ws + L.partials_off);
   p.zy = reinterpret_cast<float*>(ws + L.zy_off);
+  p.best_val = best_val;
+  p.best_idx = best_idx;
   p.status = reinterpret_cast<int32_t*>(ws);
   p.timeout_ns = g_timeout_ns;
-  const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_FWD], p.num_units));
+  const bool score = best_val != nullptr;
+  const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[score ? MODE_SCORE : MODE_FWD], p.num_units));
   KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, 2.0 * T * Hd * V,
-                 2.0 * (T * Hd + V * Hd) + 8.0 * n_split * T + 4.0 * T);
-  gemm_kernel<MODE_FWD><<<grid, kThreads, smem_bytes_for(MODE_FWD), s>>>(p);
+                 2.0 * (T * Hd + V * Hd) + (score ? 16.0 : 8.0) * n_split * T + 4.0 * T);
+  if (score)
+    gemm_kernel<MODE_SCORE><<<grid, kThreads, smem_bytes_for(MODE_SCORE), s>>>(p);
+  else
+    gemm_kernel<MODE_FWD><<<grid, kThreads, smem_bytes_for(MODE_FWD), s>>>(p);
   ks.done();
   if ((st = check_launch("fwd_logits_lse")) != FLCE_OK) return st;
   *L_out = L;
@@ -655,6 +667,49 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
   FwdLayout L;
   if ((st = launch_logits_lse(dev, s, H, W, targets, T, Hd, V, 0, ignore_index, ws, &L)) != FLCE_OK) return st;
   return launch_finalize_reduce(s, ws, L, targets, T, V, ignore_index, reduction, loss, lse, logp, n_valid);
+}
+
+size_t flce_score_workspace_size(int64_t T, int64_t Hd, int64_t V) {
+  (void)Hd;
+  if (T < 0 || V < 1) return 0;
+  const FwdLayout L = fwd_layout(T, kMaxSplit);
+  return L.total + 2 * align_up(sizeof(float) * kMaxSplit * static_cast<size_t>(L.part_stride), 256);
+}
+
+flce_status flce_score(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
+                       int64_t ignore_index, float* logp, float* lse, int64_t* argmax, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, FLCE_REDUCTION_NONE);
+  if (st != FLCE_OK) return st;
+  if (T > 0 && !logp) return fail(FLCE_ERR_INVALID_ARG, "logp is NULL");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (workspace_bytes < flce_score_workspace_size(T, Hd, V))
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
+                flce_score_workspace_size(T, Hd, V));
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  if (T == 0) return FLCE_OK;
+  const FwdLayout Lmax = fwd_layout(T, kMaxSplit);
+  const size_t best_bytes = align_up(sizeof(float) * kMaxSplit * static_cast<size_t>(Lmax.part_stride), 256);
+  float* best_val = reinterpret_cast<float*>(ws + Lmax.total);
+  int32_t* best_idx = reinterpret_cast<int32_t*>(ws + Lmax.total + best_bytes);
+  FwdLayout L;
+  if ((st = launch_logits_lse(dev, s, H, W, targets, T, Hd, V, 0, ignore_index, ws, &L, best_val, best_idx)) !=
+      FLCE_OK)
+    return st;
+  KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (16.0 * L.n_split + 4 + 8 + 4 + 4 + 8) * T);
+  score_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(
+      reinterpret_cast<const float2*>(ws + L.partials_off), reinterpret_cast<const float*>(ws + L.zy_off), best_val,
+      best_idx, targets, static_cast<int>(T), static_cast<int>(V), ignore_index, L.n_split,
+      static_cast<int>(L.part_stride), lse, logp, argmax, reinterpret_cast<int32_t*>(ws));
+  ks.done();
+  return check_launch("score_finalize");
 }
 
 size_t flce_combine_workspace_size(int64_t T, int32_t n_shards) {

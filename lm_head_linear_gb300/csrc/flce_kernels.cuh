@@ -70,14 +70,17 @@ constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-enum Mode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DHW = 2 };
+enum Mode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DHW = 2, MODE_SCORE = 3 };
+
+// MODE_SCORE is MODE_FWD plus a per-row argmax of the logits.
+__host__ __device__ constexpr bool is_forward(int mode) { return mode == MODE_FWD || mode == MODE_SCORE; }
 
 // Device status codes (match flce_status in include/flce.h).
 constexpr int kStatusTargetRange = 6;
 constexpr int kStatusTimeout = 7;
 
 __host__ __device__ constexpr int smem_bytes_for(int mode) {
-  return 1024 + NSTAGE * STAGE_BYTES + (mode == MODE_FWD ? 0 : STAGING_BYTES) + kSmemTail;
+  return 1024 + NSTAGE * STAGE_BYTES + (is_forward(mode) ? 0 : STAGING_BYTES) + kSmemTail;
 }
 static_assert(smem_bytes_for(MODE_DHW) <= 232448, "shared memory per CTA");
 static_assert(kBarriers * 8 + 8 + kTileRing * 4 <= kSmemTail, "smem tail");
@@ -113,6 +116,8 @@ struct GemmParams {
   const float* g;        // MODE_DZ
   float2* partials;      // MODE_FWD [n_split][part_stride] of (max*log2e, sum of 2^(z*log2e - max))
   float* zy;             // MODE_FWD [T] target logit
+  float* best_val;       // MODE_SCORE [n_split][part_stride]: largest logit of the row's vocab range
+  int32_t* best_idx;     // MODE_SCORE [n_split][part_stride]: its global vocab id (lowest on ties)
   int32_t* tile_counter; // MODE_DHW: zero before the launch
   int32_t* status;
   uint64_t timeout_ns;
@@ -129,7 +134,7 @@ struct Unit {
 template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, uint32_t rank) {
   Unit r;
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (is_forward(MODE)) {
     // split-major order: pairs running side by side share a vocab range, so
     // they walk the same W tiles at about the same time and reuse them in L2.
     const int split = u / p.num_m_pairs;
@@ -186,7 +191,7 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   s.stages = base;
   s.staging = base + NSTAGE * STAGE_BYTES;
-  uint8_t* tail = s.staging + (MODE == MODE_FWD ? 0 : STAGING_BYTES);
+  uint8_t* tail = s.staging + (is_forward(MODE) ? 0 : STAGING_BYTES);
   s.bars = reinterpret_cast<uint64_t*>(tail);
   s.tmem_slot = reinterpret_cast<uint32_t*>(tail + kBarriers * 8);
   s.abort_flag = reinterpret_cast<volatile int*>(tail + kBarriers * 8 + 4);
@@ -485,8 +490,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
     bool have_zy = false;
     int y = -1;
     float gt = 0.0f, lse2 = 0.0f;
+    float best = -INFINITY;
+    int best_col = -1;
     // y: the target's local vocab column when this launch's vocab rows own it, else -1
-    if constexpr (MODE == MODE_FWD) {
+    if constexpr (is_forward(MODE)) {
       if (t_local < p.rows) {
         const int64_t yy = p.targets[t_local] - p.vocab_offset;
         if (p.targets[t_local] != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
@@ -511,7 +518,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
       const uint32_t tcol = lane_addr + acc * BN;
 
       if (active) {
-        if constexpr (MODE == MODE_FWD) {
+        if constexpr (is_forward(MODE)) {
           const int n0 = nb * BN;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
@@ -533,6 +540,17 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
             float mx = v[0];
 #pragma unroll
             for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
+            if constexpr (MODE == MODE_SCORE) {
+              // strictly larger: equal values keep the earlier (lower) column
+              if (mx > best) {
+                int jj = 0;
+#pragma unroll
+                for (int j = 31; j >= 0; --j)
+                  if (v[j] == mx) jj = j;
+                best = mx;
+                best_col = col0 + jj;
+              }
+            }
             const float m_new = fmaxf(m_run, mx * kLog2e);
             float acc_s = 0.0f;
 #pragma unroll
@@ -550,10 +568,15 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
       if (acc == 0) acc_phase ^= 1u;
     }
 
-    if constexpr (MODE == MODE_FWD) {
+    if constexpr (is_forward(MODE)) {
       if (ok && t_local < p.rows) {
         p.partials[static_cast<size_t>(un.split) * p.part_stride + t_local] = make_float2(m_run, s_run);
         if (have_zy) p.zy[t_local] = zy;
+        if constexpr (MODE == MODE_SCORE) {
+          p.best_val[static_cast<size_t>(un.split) * p.part_stride + t_local] = best;
+          p.best_idx[static_cast<size_t>(un.split) * p.part_stride + t_local] =
+              static_cast<int32_t>(p.vocab_offset + best_col);
+        }
       }
     }
   }
@@ -710,7 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&p.tmA);
     ptx::prefetch_tmap(&p.tmB);
-    if (MODE != MODE_FWD) ptx::prefetch_tmap(&p.tmOut);
+    if (!is_forward(MODE)) ptx::prefetch_tmap(&p.tmOut);
     if (MODE == MODE_DHW) {
       ptx::prefetch_tmap(&p.tmA2);
       ptx::prefetch_tmap(&p.tmB2);
@@ -831,6 +854,40 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(const Fi
     p.block_sum[blockIdx.x] = sh_sum[0];
     p.block_count[blockIdx.x] = sh_cnt[0];
   }
+}
+
+// Scoring: per row, lse and logp as fwd_finalize_kernel (no loss reduction)
+// and the argmax merged over the vocab ranges in order (lowest id on ties).
+__global__ void __launch_bounds__(kFinalizeThreads) score_finalize_kernel(
+    const float2* partials, const float* zy, const float* best_val, const int32_t* best_idx, const int64_t* targets,
+    int T, int V, int64_t ignore_index, int n_split, int part_stride, float* lse_out, float* logp_out,
+    int64_t* argmax_out, int32_t* status) {
+  const int t = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  if (t >= T) return;
+  float M = -INFINITY;
+  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, partials[static_cast<size_t>(sp) * part_stride + t].x);
+  float S = 0.0f;
+  float bv = -INFINITY;
+  int32_t bi = 0;
+  for (int sp = 0; sp < n_split; ++sp) {
+    const size_t i = static_cast<size_t>(sp) * part_stride + t;
+    const float2 pr = partials[i];
+    S += pr.y * exp2f(pr.x - M);
+    if (best_val[i] > bv) {
+      bv = best_val[i];
+      bi = best_idx[i];
+    }
+  }
+  const float lse = (M + log2f(S)) * kLn2;
+  const int64_t y = targets[t];
+  bool valid = y != ignore_index;
+  if (valid && (y < 0 || y >= V)) {
+    raise_status(status, kStatusTargetRange);
+    valid = false;
+  }
+  if (lse_out) lse_out[t] = lse;
+  logp_out[t] = valid ? zy[t] - lse : 0.0f;
+  if (argmax_out) argmax_out[t] = bi;
 }
 
 // Vocab shard forward: per row, merge the shard's split partials into the

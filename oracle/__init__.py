@@ -10,6 +10,7 @@ method's arithmetic).
 
 from .flce_oracle import (  # noqa: F401
     ForwardResult,
+    argmax_rows,
     backward,
     dW_rows,
     forward,

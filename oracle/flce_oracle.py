@@ -236,6 +236,26 @@ def shard_partials(H: np.ndarray, W_shard: np.ndarray, targets: np.ndarray, voca
     return lse, zy
 
 
+def argmax_rows(H: np.ndarray, W: np.ndarray, row_block: int = 256):
+    """Greedy token per row: argmax_v z_{t,v} (lowest id on ties) and the gap between
+    the largest and the second-largest logit (at another id) of the row."""
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    T, V = H.shape[0], W.shape[0]
+    idx = np.zeros(T, dtype=np.int64)
+    gap = np.full(T, np.inf)
+    for r0 in range(0, T, row_block):
+        r1 = min(T, r0 + row_block)
+        Z = logits(H[r0:r1], W)
+        i = np.argmax(Z, axis=1)
+        idx[r0:r1] = i
+        if V > 1:
+            top = Z[np.arange(r1 - r0), i]
+            Z[np.arange(r1 - r0), i] = -np.inf
+            gap[r0:r1] = top - Z.max(axis=1)
+    return idx, gap
+
+
 def naive_logits_bytes(T: int, V: int, bytes_per_elem: int, copies: int = 1) -> int:
     """Bytes of ``copies`` dense [T x V] logits tensors (section 3 of the page;
     section 2.3 Step 1 of the Megatron-Lite / bumblebee post)."""
@@ -243,7 +263,7 @@ def naive_logits_bytes(T: int, V: int, bytes_per_elem: int, copies: int = 1) -> 
 
 
 __all__ = [
-    "ForwardResult", "backward", "dW_rows", "forward", "logits", "naive_logits_bytes",
+    "ForwardResult", "argmax_rows", "backward", "dW_rows", "forward", "logits", "naive_logits_bytes",
     "sampled_rows", "shard_partials", "upstream_grad", "valid_mask", "REDUCTIONS",
 ]
 

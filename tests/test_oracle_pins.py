@@ -299,11 +299,32 @@ def pin_vocab_shards():
     assert np.array_equal(owners, valid.astype(int))
 
 
+def pin_argmax():
+    """Greedy token: brute force on a tiny case, lowest id among exact ties, and the
+    top-2 gap; permuting the vocabulary permutes the answer."""
+    H, W, y = _rand_case(17, T=6, Hd=5, V=23, n_ignore=0)
+    idx, gap = fo.argmax_rows(H, W)
+    for t in range(6):
+        z = [sum(H[t][k] * W[v][k] for k in range(5)) for v in range(23)]
+        best = max(range(23), key=lambda v: (z[v], -v))
+        assert idx[t] == best
+        second = max(z[v] for v in range(23) if v != best)
+        assert abs(gap[t] - (z[best] - second)) < 1e-12
+    W2 = W.copy()
+    W2[[4, 17]] = 3.0  # two identical rows far above the rest for rows with a positive sum
+    i2, g2 = fo.argmax_rows(H, W2)
+    pos = H.sum(axis=1) > 0.5
+    assert np.all(i2[pos] == 4) and np.all(g2[pos] == 0.0)
+    pv = np.random.default_rng(1).permutation(23)
+    i3, _ = fo.argmax_rows(H, W[pv])
+    assert np.array_equal(pv[i3], idx)
+
+
 PINS = [
     pin_w_zero_closed_form, pin_vocab_of_one, pin_torch_library, pin_finite_differences,
     pin_brute_force_tiny, pin_shift_invariance_and_overflow, pin_gradient_sums_vanish,
     pin_ignored_rows, pin_reductions_agree, pin_permutation_equivariance,
-    pin_pages_memory_arithmetic, pin_sampled_paths, pin_vocab_shards,
+    pin_pages_memory_arithmetic, pin_sampled_paths, pin_vocab_shards, pin_argmax,
 ]
 
 
