@@ -121,6 +121,24 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(x, device=None):
+    """Max of a float over the ranks of the default process group (x itself when
+    there is none).  NCCL reduces a tensor on `device`, gloo one on the CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank, world, max_ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (max_ms / 1000.0)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -230,11 +248,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dev)
 
     for _ in range(args.warmup):
         step(H, W, y, dloss)
@@ -260,7 +274,7 @@ def run_ours(args):
     kstats = flce.flce_profile_collect()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1))
     ms_step = ms_total / args.steps
-    value = world * T * args.steps / (ms_total / 1000.0)
+    value = whole_job_tokens_per_s(T * args.steps, world, ms_total)
     gpu_launches = sum(v["launches"] for v in kstats.values())
 
     # ---- end to end through the public API with host buffers.  Every step copies its
@@ -320,7 +334,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))
     h2d = H_h.numel() * 2 + W_h.numel() * 2 + y_h.numel() * 8 + dl_h.numel() * 4
     d2h = loss_h.numel() * 4 + dH_h.numel() * 2 + dW_h.numel() * 4
-    e2e = {"value": world * T * e2e_steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+    e2e = {"value": whole_job_tokens_per_s(T * e2e_steps, world, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
     if rank != 0:

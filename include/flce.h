@@ -218,6 +218,13 @@ FLCE_API flce_status flce_backward_shard(const float* dloss, const void* H, cons
  * made with `workspace` into *out (an flce_status value). */
 FLCE_API flce_status flce_read_device_status(const void* workspace, void* stream, int32_t* out);
 
+/* Self-test of the kernels' bounded waits (no counterpart on the pages): one
+ * thread waits on an mbarrier that nothing ever completes, with the same
+ * bounded wait every GEMM role uses, and writes FLCE_ERR_TIMEOUT to the status
+ * word of `workspace` (>= 256 bytes) once `timeout_ns` (1e6 .. 1e10) has
+ * passed.  Read it with flce_read_device_status(); the context stays usable. */
+FLCE_API flce_status flce_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 FLCE_API const char* flce_status_string(int32_t status);
 

@@ -14,7 +14,8 @@ from typing import Optional
 
 import torch
 
-from . import build as _build
+# Where `python -m lm_head_linear_gb300.build` writes the library.
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libflce.so")
 
 REDUCTIONS = {"none": 0, "mean": 1, "sum": 2}
 STATUS_NAMES = {
@@ -43,6 +44,7 @@ SIGNATURES = {
                                    ctypes.c_size_t, _P]),
     "flce_backward": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
+    "flce_selftest_wait_timeout": (_I32, [_P, ctypes.c_uint64, _P]),
     "flce_status_string": (ctypes.c_char_p, [_I32]),
     "flce_last_error": (ctypes.c_char_p, []),
     "flce_abi_version": (_I32, []),
@@ -68,7 +70,7 @@ _LIB: Optional[ctypes.CDLL] = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    return LIB_PATH
 
 
 def load_library() -> ctypes.CDLL:
@@ -288,6 +290,14 @@ def flce_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     v = ctypes.c_int32(-1)
     _check(lib.flce_read_device_status(_ptr(workspace), _stream_handle(stream), ctypes.byref(v)))
     return int(v.value)
+
+
+def flce_selftest_wait_timeout(timeout_ns: int, device=None, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the device status it produced."""
+    lib = load_library()
+    ws = torch.empty(256, dtype=torch.uint8, device=device or torch.device("cuda"))
+    _check(lib.flce_selftest_wait_timeout(_ptr(ws), int(timeout_ns), _stream_handle(stream)))
+    return flce_read_device_status(ws, stream)
 
 
 def flce_set_wait_timeout_ns(ns: int):

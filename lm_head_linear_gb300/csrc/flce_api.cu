@@ -630,6 +630,21 @@ int64_t flce_backward_chunk_tokens(int64_t T, int64_t Hd, int64_t V, size_t work
   return c < 128 ? 0 : c;
 }
 
+flce_status flce_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream) {
+  if (!workspace) return fail(FLCE_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull)
+    return fail(FLCE_ERR_INVALID_ARG, "timeout_ns must lie in [1e6, 1e10]");
+  DeviceInfo* dev = nullptr;
+  flce_status st = device_info(&dev);
+  if (st != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemsetAsync(workspace, 0, kHeaderBytes, s));
+  wait_selftest_kernel<<<1, 1, 0, s>>>(static_cast<int32_t*>(workspace), timeout_ns);
+  return check_launch("wait_selftest");
+}
+
 flce_status flce_read_device_status(const void* workspace, void* stream, int32_t* out) {
   if (!workspace || !out) return fail(FLCE_ERR_INVALID_ARG, "workspace or out is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -67,6 +67,7 @@ constexpr int kTileRing = 8;                    // MODE_DHW: tile indices in fli
 constexpr int kBarriers = 2 * NSTAGE + 5 + 2 * kTileRing;
 constexpr int kSmemTail = 512;                  // barriers + TMEM slot + abort flag + tile ring
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
+constexpr uint64_t kAbortSettleNs = 200000ull;   // 200 us: far longer than any TMA load takes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -774,6 +775,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       epilogue_loop<MODE>(p, s, tmem_base, warp, lane, rank);
   }
 
+  // After an abort the odd CTA's loads may not have been consumed (they are
+  // counted on the even CTA's barriers): give any TMA write still in flight
+  // time to land before shared memory is released.
+  if (warp == 0 && *s.abort_flag) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < kAbortSettleNs) {
+    }
+  }
   // No CTA leaves while its peer may still signal its barriers or use the
   // pair's TMEM.
   ptx::tc_fence_before();
@@ -994,6 +1003,19 @@ __global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* d
     const bool valid = (y != ignore_index) && y >= 0 && y < V;
     g[t] = valid ? (reduction == 0 ? dloss[t] : scalar) : 0.0f;
   }
+}
+
+// ----------------------------------------------------------------------------- self-test of the bounded wait
+// One thread waits, with the same bounded wait the GEMMs use, on an mbarrier
+// that nothing arrives on, and records FLCE_ERR_TIMEOUT in the status word
+// when the limit runs out (and 0 if the wait ever succeeded, which it cannot).
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = ptx::smem_u32(&bar);
+  ptx::mbar_init(b, 1);
+  ptx::fence_barrier_init();
+  const bool ok = ptx::wait_bounded(b, 0, timeout_ns, nullptr);
+  *status = ok ? 0 : kStatusTimeout;
 }
 
 }  // namespace flce
