@@ -258,19 +258,42 @@ def run_ours(args):
         if st != 0:
             raise RuntimeError(f"device status {st} after the warm-up {k}")
 
-    # ---- device-resident timed region (value); per-kernel events for the roofline
+    # ---- device-resident timed region (value); per-kernel events for the roofline.
+    # With --graph the step is captured once into a CUDA graph and the timed loop
+    # replays it (for launch-bound shapes); the per-kernel events then come from an
+    # eager pass of the same number of steps.
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                step(H, W, y, dloss)
+        stream.wait_stream(cap)
+        for _ in range(args.warmup):
+            graph.replay()
+        barrier()
     flce.flce_profile_collect()
-    flce.flce_profile_enable(True)
+    flce.flce_profile_enable(graph is None)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         barrier()
         ev0.record(stream)
         for _ in range(args.steps):
-            step(H, W, y, dloss)
+            if graph is not None:
+                graph.replay()
+            else:
+                step(H, W, y, dloss)
         ev1.record(stream)
         barrier()
     flce.flce_profile_enable(False)
+    if graph is not None:
+        flce.flce_profile_enable(True)
+        for _ in range(args.steps):
+            step(H, W, y, dloss)
+        flce.flce_profile_enable(False)
     kstats = flce.flce_profile_collect()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1))
     ms_step = ms_total / args.steps
@@ -362,7 +385,8 @@ def run_ours(args):
                    "backward_chunk_tokens": flce.flce_backward_chunk_tokens(T, Hd, V, bws.numel()),
                    "l2": "inputs larger than L2 (H %.0f MB + W %.0f MB > 129 MB), no flush" % (
                        T * Hd * 2 / 1e6, V * Hd * 2 / 1e6),
-                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "launch": "cuda graph replay" if args.graph else "eager"},
         "tflops": tflops,
         "frac_of_bf16_peak": {"burst": tflops / float(peaks.get("bf16_tflops", 1)),
                               "sustained": tflops / peak, "source": peak_src},
@@ -398,6 +422,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of one step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
