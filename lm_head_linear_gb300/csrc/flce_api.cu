@@ -247,13 +247,14 @@ int64_t default_chunk(int64_t T) {
   return std::min<int64_t>(c, kDefaultChunk);
 }
 
-// Vocab ranges per token block for the forward: the count whose units spread
-// most evenly over `grid` persistent CTAs (ties go to fewer ranges).
+// Vocab ranges per token pair for the forward: the even count (the forward
+// walks ranges two at a time) whose units spread most evenly over `grid`
+// persistent SM pairs, ties going to fewer ranges; 1 when V has a single tile.
 int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
   int best = 1;
   double best_eff = -1.0;
   const int max_split = static_cast<int>(std::min<int64_t>(kMaxSplit, n_blocks));
-  for (int ns = 1; ns <= max_split; ++ns) {
+  for (int ns = 2; ns <= max_split; ns += 2) {
     const int64_t units = m_blocks * ns;
     const int64_t per_unit = cdiv(n_blocks, ns);
     const int64_t waves = cdiv(units, grid);

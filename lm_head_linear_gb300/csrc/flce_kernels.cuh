@@ -136,12 +136,19 @@ template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, uint32_t rank) {
   Unit r;
   if constexpr (is_forward(MODE)) {
-    // split-major order: pairs running side by side share a vocab range, so
-    // they walk the same W tiles at about the same time and reuse them in L2.
-    const int split = u / p.num_m_pairs;
+    // Vocab ranges are taken two at a time (when n_split is even): units
+    // (token pair, range 2g), (token pair, range 2g + 1), next token pair, ...
+    // Pairs running side by side then walk two ranges' W tiles together and
+    // hold half as many H blocks, which keeps both in L2 (forward DRAM reads
+    // 25 GB -> 10 GB at 65,536 x 2048 x 124,160).
+    const int G = (p.n_split % 2 == 0) ? 2 : 1;
+    const int gsz = G * p.num_m_pairs;
+    const int grp = u / gsz;
+    const int rr = u - grp * gsz;
+    const int split = grp * G + rr % G;
     const int base = p.num_n_blocks / p.n_split;
     const int rem = p.num_n_blocks % p.n_split;
-    r.m_blk = 2 * (u - split * p.num_m_pairs) + static_cast<int>(rank);
+    r.m_blk = 2 * (rr / G) + static_cast<int>(rank);
     r.split = split;
     r.n_lo = split * base + min(split, rem);
     r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
