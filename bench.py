@@ -48,10 +48,16 @@ def load_peaks():
 
 
 def kernel_source_sha():
+    """Hash of the library's code with comments and whitespace removed, so that
+    DRAM counters stay attached to the code they were taken on."""
+    import re
     h = hashlib.sha256()
     for f in ("csrc/flce_kernels.cuh", "csrc/ptx.cuh", "csrc/flce_api.cu"):
-        with open(os.path.join(ROOT, "lm_head_linear_gb300", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "lm_head_linear_gb300", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

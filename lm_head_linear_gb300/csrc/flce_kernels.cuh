@@ -17,6 +17,8 @@
 //             Tiles are handed out by a global atomic counter, the long dH
 //             tiles first, so the short dW tiles fill the SMs that the dH
 //             tiles leave idle at the end of their last wave.
+//   MODE_SCORE MODE_FWD that also keeps each row's largest logit and its id
+//             (the greedy token), for scoring without a loss.
 //
 // SM pairs: every kernel runs as clusters of two CTAs on two SMs that compute
 // one 256 x 256 output tile together with cta_group::2 MMAs (M = 256, N = 256,
