@@ -10,7 +10,7 @@ import torch
 import lm_head_linear_gb300 as flce
 from workloads import generate
 
-from gpu_helpers import run
+from gpu_helpers import run, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -33,3 +33,35 @@ def test_selftest_rejects_out_of_range_limits(cuda_device):
     with pytest.raises(flce.FlceError) as e:
         flce.flce_selftest_wait_timeout(10, device=cuda_device)
     assert e.value.status == 1
+
+
+def test_gemm_abort_path_reports_timeout(cuda_device):
+    """One 256 x 256 forward tile with K = Hd = 524,288 keeps one SM pair's tensor
+    cores busy for ~2 ms.  With the wait limit at 1 ms the epilogue's wait for that
+    accumulator runs out inside a legitimate GEMM: the kernel must take its abort path
+    (abort flag, drains, TMEM freed), report FLCE_ERR_TIMEOUT and leave the context
+    usable.  With the default limit the same shape matches the oracle."""
+    import oracle
+    from gpu_helpers import TOL_TOKEN
+    inp = generate("tiny", T=256, Hd=524288, V=256)
+    H, W, y, _ = to_device(inp, cuda_device)
+    try:
+        flce.flce_set_wait_timeout_ns(1_000_000)
+        _, _, _, _, ws = flce.flce_forward(H, W, y)
+        assert flce.flce_read_device_status(ws) == 7
+    finally:
+        flce.flce_set_wait_timeout_ns(4_000_000_000)
+    loss, lse, logp, n_valid, ws = flce.flce_forward(H, W, y)
+    assert flce.flce_read_device_status(ws) == 0
+    # At this K the fp32 tensor-core accumulation (one rounding per K = 16 step, 32,768
+    # steps) is no longer inside the per-token tolerance; bound it by one ulp of the
+    # row's largest |logit| per step.
+    H64, W64 = inp.H64(), inp.W64()
+    ref = oracle.forward(H64, W64, inp.targets, inp.ignore_index, "mean")
+    zmax = np.abs(oracle.logits(H64, W64)).max(axis=1)
+    ulp = 2.0 ** (np.floor(np.log2(zmax)) - 23)
+    bound = (inp.Hd / 16) * ulp + TOL_TOKEN
+    assert np.all(np.abs(lse.cpu().numpy() - ref.lse) <= bound)
+    small = generate("tiny", T=300, Hd=128, V=1000)
+    out = run(small, cuda_device)
+    assert out["fwd_status"] == 0 and out["bwd_status"] == 0

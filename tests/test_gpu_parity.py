@@ -51,6 +51,13 @@ def test_full_oracle(case, cuda_device):
     _full_check(inp, run(inp, cuda_device))
 
 
+def test_wide_hidden_16384(cuda_device):
+    """Hd = 16,384 (1,024 accumulation steps of K = 16 per logit): still inside the
+    per-token and gradient tolerances."""
+    inp = generate("medium", T=300, Hd=16384, V=2000)
+    _full_check(inp, run(inp, cuda_device))
+
+
 def test_many_token_chunks(cuda_device):
     """A workspace sized for 128-token chunks: dW accumulates over 8 chunks in order."""
     inp = generate("medium", T=1000, Hd=256, V=5000)
