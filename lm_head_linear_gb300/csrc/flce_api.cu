@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdarg>
@@ -159,12 +160,15 @@ cudaEvent_t take_event() {
   return e;
 }
 
-// Brackets one launch with events on its stream while profiling is enabled.
+// Brackets one launch with an NVTX range named after the kernel (seen by any
+// attached profiler) and, while profiling is enabled, with events on its stream.
 struct KernelScope {
   bool on = false;
+  bool nvtx = true;
   LaunchRecord rec{};
   cudaStream_t stream;
   KernelScope(int kind, cudaStream_t s, double flops, double bytes) : stream(s) {
+    nvtxRangePushA(flce_kernel_name(kind));
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on) return;
     on = true;
@@ -175,7 +179,14 @@ struct KernelScope {
     rec.stop = take_event();
     cudaEventRecord(rec.start, s);
   }
+  ~KernelScope() {
+    if (nvtx) nvtxRangePop();
+  }
   void done() {
+    if (nvtx) {
+      nvtxRangePop();
+      nvtx = false;
+    }
     if (!on) return;
     cudaEventRecord(rec.stop, stream);
     std::lock_guard<std::mutex> lk(g_prof_mu);
