@@ -34,7 +34,7 @@
  *   - H and W are bf16, row-major: H [T, Hd], W [V, Hd], each row contiguous.
  *     Hd must be a positive multiple of 64; H, W, dH and dW must be 16-byte
  *     aligned; the workspace 256-byte aligned.  T may be 0.  V >= 1.
- *     T, V < 2^31.
+ *     T, V < 2^30.
  *   - Rows whose target equals ignore_index contribute zero loss and zero
  *     gradient and are not counted in n_valid.  ignore_index must lie outside
  *     [0, V).

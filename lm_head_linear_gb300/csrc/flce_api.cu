@@ -39,6 +39,8 @@ constexpr size_t kHeaderBytes = 256;  // status word and spare scalars at the st
 constexpr int kMaxSplit = 16;         // forward: vocab ranges per token block
 constexpr int64_t kDefaultChunk = 8192;
 constexpr int32_t kMaxShards = 64;    // vocab shards one combine call merges
+// T and V bound: tile coordinates (block * 128 + row) stay inside int32 with room to spare.
+constexpr int64_t kMaxRows = int64_t(1) << 30;
 
 uint64_t g_timeout_ns = 4000000000ull;
 
@@ -281,8 +283,8 @@ int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
 
 flce_status check_common(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
                          int64_t ignore_index, int32_t reduction) {
-  if (T < 0 || T >= (int64_t(1) << 31)) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
-  if (V < 1 || V >= (int64_t(1) << 31)) return fail(FLCE_ERR_INVALID_ARG, "V = %lld out of range", (long long)V);
+  if (T < 0 || T >= kMaxRows) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
+  if (V < 1 || V >= kMaxRows) return fail(FLCE_ERR_INVALID_ARG, "V = %lld out of range", (long long)V);
   if (Hd < 1 || Hd >= (int64_t(1) << 24)) return fail(FLCE_ERR_INVALID_ARG, "Hd = %lld out of range", (long long)Hd);
   if (Hd % 64 != 0) return fail(FLCE_ERR_UNSUPPORTED, "Hd = %lld is not a multiple of 64", (long long)Hd);
   if (reduction < 0 || reduction > 2) return fail(FLCE_ERR_INVALID_ARG, "unknown reduction %d", reduction);
@@ -410,7 +412,7 @@ flce_status launch_finalize_reduce(cudaStream_t s, uint8_t* ws, const FwdLayout&
 }
 
 flce_status check_shard(int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t ignore_index) {
-  if (V_total < 1 || V_total >= (int64_t(1) << 31))
+  if (V_total < 1 || V_total >= kMaxRows)
     return fail(FLCE_ERR_INVALID_ARG, "V_total = %lld out of range", (long long)V_total);
   if (V_shard < 1 || vocab_offset < 0 || vocab_offset + V_shard > V_total)
     return fail(FLCE_ERR_INVALID_ARG, "shard [%lld, %lld) does not lie inside [0, V_total = %lld)",
@@ -784,8 +786,8 @@ flce_status flce_combine_shards(const float* shard_lse, const float* shard_zy, i
                                 void* workspace, size_t workspace_bytes, void* stream) {
   if (n_shards < 1 || n_shards > kMaxShards)
     return fail(FLCE_ERR_INVALID_ARG, "n_shards = %d outside [1, %d]", n_shards, kMaxShards);
-  if (T < 0 || T >= (int64_t(1) << 31)) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
-  if (V_total < 1 || V_total >= (int64_t(1) << 31))
+  if (T < 0 || T >= kMaxRows) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
+  if (V_total < 1 || V_total >= kMaxRows)
     return fail(FLCE_ERR_INVALID_ARG, "V_total = %lld out of range", (long long)V_total);
   if (reduction < 0 || reduction > 2) return fail(FLCE_ERR_INVALID_ARG, "unknown reduction %d", reduction);
   if (ignore_index >= 0 && ignore_index < V_total)
