@@ -126,6 +126,19 @@ FLCE_API flce_status flce_backward(const float* dloss, const void* H, const void
                                    int32_t reduction, void* dH, float* dW, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Backward with a gradient on the logp output as well.  RL trainers build
+ * their objective from the per-token log-probabilities (policy-gradient and
+ * ratio terms), so the upstream gradient can arrive on logp instead of, or as
+ * well as, on the loss.  On valid rows logp_t = -loss_t, so dlogp_t enters the
+ * per-token weight as g_t = (gradient of the loss output at t) - dlogp_t.
+ *   dloss   as flce_backward, or NULL (no gradient on the loss output)
+ *   dlogp   [T] fp32, or NULL (no gradient on logp); ignored rows get g_t = 0
+ * Everything else as flce_backward. */
+FLCE_API flce_status flce_backward_logp(const float* dloss, const float* dlogp, const void* H, const void* W,
+                                        const int64_t* targets, const float* lse, int64_t T, int64_t Hd, int64_t V,
+                                        int64_t ignore_index, int32_t reduction, void* dH, float* dW,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Forward without any allocation by the caller or the library.  The pages
  * have no counterpart to this entry point; it exists for callers that cannot
  * allocate device memory at the point where they need the loss: code whose

@@ -27,5 +27,6 @@ from .binding import (  # noqa: F401
     flce_set_wait_timeout_ns,
     library_path,
     linear_cross_entropy,
+    linear_log_probs,
     load_library,
 )

@@ -43,6 +43,8 @@ SIGNATURES = {
     "flce_backward_shard": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32, _P, _P, _P,
                                    ctypes.c_size_t, _P]),
     "flce_backward": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_backward_logp": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, ctypes.c_size_t,
+                                  _P]),
     "flce_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "flce_selftest_wait_timeout": (_I32, [_P, ctypes.c_uint64, _P]),
     "flce_status_string": (ctypes.c_char_p, [_I32]),
@@ -177,19 +179,29 @@ def flce_forward(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore
     return loss, lse, logp, n_valid, ws
 
 
-def flce_backward(dloss: torch.Tensor, H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
-                  ignore_index: int = -100, reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
-                  stream=None, out: Optional[dict] = None):
-    """Run ``flce_backward``; returns ``(dH bf16 [T, Hd], dW fp32 [V, Hd], workspace)``."""
+def flce_backward(dloss: Optional[torch.Tensor], H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                  lse: torch.Tensor, ignore_index: int = -100, reduction: str = "mean",
+                  workspace: Optional[torch.Tensor] = None, stream=None, out: Optional[dict] = None,
+                  dlogp: Optional[torch.Tensor] = None):
+    """Run ``flce_backward`` (or ``flce_backward_logp`` when ``dlogp``, a [T] gradient on
+    the logp output, is given; ``dloss`` may then be None).  Returns
+    ``(dH bf16 [T, Hd], dW fp32 [V, Hd], workspace)``."""
     _check_inputs(H, W, targets)
     lib = load_library()
     T, Hd = H.shape
     V = W.shape[0]
     red = REDUCTIONS[reduction]
     dev = H.device
-    dloss = dloss.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
-    if dloss.numel() != (T if red == 0 else 1):
-        raise ValueError("dloss must have one element (mean / sum) or T elements (none)")
+    if dloss is None and dlogp is None:
+        raise ValueError("give dloss, dlogp or both")
+    if dloss is not None:
+        dloss = dloss.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
+        if dloss.numel() != (T if red == 0 else 1):
+            raise ValueError("dloss must have one element (mean / sum) or T elements (none)")
+    if dlogp is not None:
+        dlogp = dlogp.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
+        if dlogp.numel() != T:
+            raise ValueError("dlogp must have T elements")
     lse = lse.contiguous()
     out = out or {}
     dH = out.get("dH")
@@ -200,8 +212,13 @@ def flce_backward(dloss: torch.Tensor, H: torch.Tensor, W: torch.Tensor, targets
         dW = torch.empty((V, Hd), dtype=torch.float32, device=dev)
     need = lib.flce_backward_workspace_size(T, Hd, V)
     ws = _workspace(need, dev, workspace)
-    st = lib.flce_backward(_ptr(dloss), _ptr(H), _ptr(W), _ptr(targets), _ptr(lse), T, Hd, V, int(ignore_index),
-                           red, _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream_handle(stream))
+    if dlogp is None:
+        st = lib.flce_backward(_ptr(dloss), _ptr(H), _ptr(W), _ptr(targets), _ptr(lse), T, Hd, V, int(ignore_index),
+                               red, _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream_handle(stream))
+    else:
+        st = lib.flce_backward_logp(_ptr(dloss), _ptr(dlogp), _ptr(H), _ptr(W), _ptr(targets), _ptr(lse), T, Hd, V,
+                                    int(ignore_index), red, _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                                    _stream_handle(stream))
     _check(st)
     return dH, dW, ws
 
@@ -324,10 +341,12 @@ def flce_profile_collect() -> dict:
 
 
 class LinearCrossEntropy(torch.autograd.Function):
-    """autograd wrapper: forward runs ``flce_forward``, backward ``flce_backward``.
+    """autograd wrapper: forward runs ``flce_forward``, backward ``flce_backward``
+    (``flce_backward_logp`` when a gradient reaches ``logp``).
 
-    Returns ``(loss, logp)``; ``logp`` is an output only (no gradient flows
-    through it).  The weight gradient comes back in W's dtype.
+    Returns ``(loss, logp)``; both are differentiable, so an objective built
+    from the per-token log-probabilities (e.g. ``-(adv * logp).sum()``) works.
+    The weight gradient comes back in W's dtype.
     """
 
     @staticmethod
@@ -336,7 +355,6 @@ class LinearCrossEntropy(torch.autograd.Function):
         ctx.save_for_backward(H, W, targets, lse)
         ctx.ignore_index = ignore_index
         ctx.reduction = reduction
-        ctx.mark_non_differentiable(logp)
         if reduction != "none":
             loss = loss.reshape(())
         return loss, logp
@@ -344,12 +362,16 @@ class LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dloss, dlogp):
         H, W, targets, lse = ctx.saved_tensors
-        if dloss is None:
-            dloss = torch.zeros(1 if ctx.reduction != "none" else H.shape[0], device=H.device)
-        dH, dW, _ = flce_backward(dloss, H, W, targets, lse, ctx.ignore_index, ctx.reduction)
+        dH, dW, _ = flce_backward(dloss, H, W, targets, lse, ctx.ignore_index, ctx.reduction, dlogp=dlogp)
         return dH, dW.to(W.dtype), None, None, None
 
 
 def linear_cross_entropy(H, W, targets, ignore_index: int = -100, reduction: str = "mean"):
     """Fused ``cross_entropy(H @ W.T, targets)`` without materialising the logits; returns the loss."""
     return LinearCrossEntropy.apply(H, W, targets, ignore_index, reduction)[0]
+
+
+def linear_log_probs(H, W, targets, ignore_index: int = -100):
+    """Per-token ``log p(target)`` under ``softmax(H @ W.T)`` (0 on ignored rows),
+    differentiable, without materialising the logits."""
+    return LinearCrossEntropy.apply(H, W, targets, ignore_index, "none")[1]

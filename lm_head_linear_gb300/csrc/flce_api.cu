@@ -424,12 +424,13 @@ flce_status check_shard(int64_t V_shard, int64_t vocab_offset, int64_t V_total, 
 
 // The backward over W rows [0, V) with global ids vocab_offset + row; g_t is
 // computed against the full vocabulary [0, V_total).
-flce_status backward_impl(const float* dloss, const void* H, const void* W, const int64_t* targets, const float* lse,
-                          int64_t T, int64_t Hd, int64_t V, int64_t vocab_offset, int64_t V_total,
-                          int64_t ignore_index, int32_t reduction, void* dH, float* dW, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+flce_status backward_impl(const float* dloss, const float* dlogp, const void* H, const void* W,
+                          const int64_t* targets, const float* lse, int64_t T, int64_t Hd, int64_t V,
+                          int64_t vocab_offset, int64_t V_total, int64_t ignore_index, int32_t reduction, void* dH,
+                          float* dW, void* workspace, size_t workspace_bytes, void* stream) {
   flce_status st;
-  if (!dW || (T > 0 && (!dloss || !lse || !dH))) return fail(FLCE_ERR_INVALID_ARG, "dloss, lse, dH or dW is NULL");
+  if (!dW || (T > 0 && ((!dloss && !dlogp) || !lse || !dH)))
+    return fail(FLCE_ERR_INVALID_ARG, "dloss (or dlogp), lse, dH or dW is NULL");
   if ((reinterpret_cast<uintptr_t>(dH) | reinterpret_cast<uintptr_t>(dW)) & 15)
     return fail(FLCE_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
   if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
@@ -457,8 +458,8 @@ flce_status backward_impl(const float* dloss, const void* H, const void* W, cons
 
   {
     KernelScope ks(FLCE_KERNEL_BWD_PREP, s, 0.0, 12.0 * T);
-    bwd_prep_kernel<<<1, kReduceThreads, 0, s>>>(dloss, targets, static_cast<int>(T), static_cast<int>(V_total),
-                                                 ignore_index, reduction, g, status);
+    bwd_prep_kernel<<<1, kReduceThreads, 0, s>>>(dloss, dlogp, targets, static_cast<int>(T),
+                                                 static_cast<int>(V_total), ignore_index, reduction, g, status);
     ks.done();
     if ((st = check_launch("bwd_prep")) != FLCE_OK) return st;
   }
@@ -847,8 +848,18 @@ flce_status flce_backward(const float* dloss, const void* H, const void* W, cons
                           float* dW, void* workspace, size_t workspace_bytes, void* stream) {
   flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
   if (st != FLCE_OK) return st;
-  return backward_impl(dloss, H, W, targets, lse, T, Hd, V, 0, V, ignore_index, reduction, dH, dW, workspace,
-                       workspace_bytes, stream);
+  return backward_impl(dloss, nullptr, H, W, targets, lse, T, Hd, V, 0, V, ignore_index, reduction, dH, dW,
+                       workspace, workspace_bytes, stream);
+}
+
+flce_status flce_backward_logp(const float* dloss, const float* dlogp, const void* H, const void* W,
+                               const int64_t* targets, const float* lse, int64_t T, int64_t Hd, int64_t V,
+                               int64_t ignore_index, int32_t reduction, void* dH, float* dW, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
+  if (st != FLCE_OK) return st;
+  return backward_impl(dloss, dlogp, H, W, targets, lse, T, Hd, V, 0, V, ignore_index, reduction, dH, dW,
+                       workspace, workspace_bytes, stream);
 }
 
 flce_status flce_backward_shard(const float* dloss, const void* H, const void* W_shard, const int64_t* targets,
@@ -858,8 +869,8 @@ flce_status flce_backward_shard(const float* dloss, const void* H, const void* W
   flce_status st = check_shard(V_shard, vocab_offset, V_total, ignore_index);
   if (st != FLCE_OK) return st;
   if ((st = check_common(H, W_shard, targets, T, Hd, V_shard, -1, reduction)) != FLCE_OK) return st;
-  return backward_impl(dloss, H, W_shard, targets, lse, T, Hd, V_shard, vocab_offset, V_total, ignore_index,
-                       reduction, dH_partial, dW_shard, workspace, workspace_bytes, stream);
+  return backward_impl(dloss, nullptr, H, W_shard, targets, lse, T, Hd, V_shard, vocab_offset, V_total,
+                       ignore_index, reduction, dH_partial, dW_shard, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -981,10 +981,13 @@ __global__ void __launch_bounds__(kReduceThreads) fwd_reduce_kernel(const double
 
 // ----------------------------------------------------------------------------- backward prep
 // One block: count valid rows (fixed-order tree), flag out-of-range targets,
-// then write the per-token upstream weight g_t.
-__global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* dloss, const int64_t* targets, int T,
-                                                                  int V, int64_t ignore_index, int reduction,
-                                                                  float* g, int32_t* status) {
+// then write the per-token upstream weight g_t.  dloss may be null (no loss
+// gradient); dlogp, when given, is a gradient on the logp output, and since
+// logp_t = -loss_t on valid rows it enters g_t with a minus sign.
+__global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* dloss, const float* dlogp,
+                                                                  const int64_t* targets, int T, int V,
+                                                                  int64_t ignore_index, int reduction, float* g,
+                                                                  int32_t* status) {
   __shared__ long long sh_cnt[kReduceThreads];
   long long c = 0;
   bool bad = false;
@@ -1005,12 +1008,14 @@ __global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* d
     __syncthreads();
   }
   const long long n = sh_cnt[0];
-  const float scalar = (reduction == 1) ? (n > 0 ? dloss[0] / static_cast<float>(n) : 0.0f)
-                                        : (reduction == 2 ? dloss[0] : 0.0f);
+  const float d0 = dloss ? dloss[0] : 0.0f;
+  const float scalar = (reduction == 1) ? (n > 0 ? d0 / static_cast<float>(n) : 0.0f) : (reduction == 2 ? d0 : 0.0f);
   for (int t = threadIdx.x; t < T; t += kReduceThreads) {
     const int64_t y = targets[t];
     const bool valid = (y != ignore_index) && y >= 0 && y < V;
-    g[t] = valid ? (reduction == 0 ? dloss[t] : scalar) : 0.0f;
+    float gt = reduction == 0 ? (dloss ? dloss[t] : 0.0f) : scalar;
+    if (dlogp) gt -= dlogp[t];
+    g[t] = valid ? gt : 0.0f;
   }
 }
 

@@ -234,3 +234,27 @@ def test_full_size_sampled_dW_medium(cuda_device):
     lse = out["lse"].cpu().numpy().astype(np.float64)
     assert np.max(np.abs(lse - ref.lse)) <= TOL_TOKEN
     assert abs(float(out["loss"].item()) - float(ref.loss)) <= TOL_TOKEN
+
+
+def test_gradient_through_logp(cuda_device):
+    """A policy-gradient objective built from the per-token log-probabilities,
+    J = -(adv * logp).sum() + 0.3 * loss_mean, differentiated by autograd through
+    both outputs; the oracle gets the equivalent per-token weights
+    g_t = 0.3 / N + adv_t on valid rows (since logp_t = -loss_t there)."""
+    inp = generate("rlpg", T=768, Hd=192, V=3001, n_seq=8)
+    H, W, y, _ = to_device(inp, cuda_device)
+    adv = torch.from_numpy(np.random.default_rng(3).standard_normal(768).astype(np.float32)).to(cuda_device)
+    Hr = H.clone().requires_grad_(True)
+    Wr = W.clone().float().requires_grad_(True)
+    loss, logp = flce.LinearCrossEntropy.apply(Hr, Wr.to(torch.bfloat16), y, -100, "mean")
+    J = -(adv * logp).sum() + 0.3 * loss
+    J.backward()
+    valid = inp.targets != inp.ignore_index
+    n = int(valid.sum())
+    g = np.where(valid, 0.3 / n + adv.cpu().numpy().astype(np.float64), 0.0)
+    dH_ref, dW_ref = oracle.backward(g, inp.H64(), inp.W64(), inp.targets, inp.ignore_index, "none")
+    assert rel_fro(Hr.grad.float().cpu().numpy(), dH_ref) <= TOL_GRAD
+    assert rel_fro(Wr.grad.float().cpu().numpy(), dW_ref) <= TOL_GRAD
+    lp = flce.linear_log_probs(H, W, y)
+    ref = oracle.forward(inp.H64(), inp.W64(), inp.targets, inp.ignore_index, "none")
+    assert np.max(np.abs(lp.detach().cpu().numpy() - ref.logp)) <= TOL_TOKEN
