@@ -8,9 +8,10 @@ hidden 2048 x vocab 124,160 (bf16 inputs, fp32 accumulation).
 
 Prints one JSON line.  ``value`` is whole-job tokens/s with the inputs resident
 in HBM; ``e2e`` is the same metric through the public API with the inputs in
-pinned host memory, copied in and the loss and gradients copied back inside the
-timed region.  ``--impl reference`` times the fp64 CPU oracle on the host cores
-instead (a bounded sample of the same workload).
+pinned host memory, copied in, and the loss and per-token log p(target) copied
+back, inside the timed region (dH and dW stay on the device for the optimizer).
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the op
 shards by token batches with no exchange inside it), the timed region is
@@ -256,9 +257,21 @@ def run_ours(args):
     def max_over_ranks(x):
         return reduce_max(x, dev)
 
+    # Device memory across the warm-up steps: the library allocates nothing itself, so the
+    # driver's free-memory count must not move, and the caller's buffers are the inputs,
+    # the outputs and the two workspaces (the [chunk x V] dZ block being the largest).
+    barrier()
+    free0 = torch.cuda.mem_get_info(dev)[0]
     for _ in range(args.warmup):
         step(H, W, y, dloss)
     barrier()
+    free1 = torch.cuda.mem_get_info(dev)[0]
+    chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws.numel())
+    io_bytes = sum(t.numel() * t.element_size() for t in (H, W, y, dloss, *out_f.values(), *out_b.values()))
+    memory = {"logits_copy_bytes": T * V * 2, "workspace_bytes": int(fws.numel() + bws.numel()),
+              "dz_block_bytes": 2 * chunk * ((V + 63) // 64 * 64), "io_bytes": int(io_bytes),
+              "torch_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(dev)),
+              "driver_free_delta_over_warmup_bytes": int(free0 - free1)}
     for k in ("fwd", "bwd"):
         st = flce.flce_read_device_status(fws if k == "fwd" else bws)
         if st != 0:
@@ -388,7 +401,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name if (T, Hd, V) == (wl.T, wl.Hd, wl.V) else f"{wl.name} at T={T} Hd={Hd} V={V}",
                    "T": T, "Hd": Hd, "V": V, "reduction": wl.reduction,
-                   "backward_chunk_tokens": flce.flce_backward_chunk_tokens(T, Hd, V, bws.numel()),
+                   "backward_chunk_tokens": chunk,
                    "l2": "inputs larger than L2 (H %.0f MB + W %.0f MB > 129 MB), no flush" % (
                        T * Hd * 2 / 1e6, V * Hd * 2 / 1e6),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -405,7 +418,7 @@ def run_ours(args):
         "gpu_launches": int(gpu_launches),
         "e2e": e2e,
         "clocks": clocks.summary(),
-        "peak_extra_bytes": int(fws.numel() + bws.numel()),
+        "memory": memory,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(inp, budget_s=args.cpu_seconds)

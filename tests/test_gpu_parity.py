@@ -182,11 +182,19 @@ def test_full_size_workload(name, cuda_device):
     peak_extra = torch.cuda.max_memory_allocated(cuda_device) - base
     assert out["fwd_status"] == 0 and out["bwd_status"] == 0
     T, V, Hd = inp.T, inp.V, inp.Hd
-    # never a [T x V] buffer: the workspace stays below one bf16 logits copy, and so does
-    # everything allocated beyond the inputs and the dH / dW outputs
+    # never a [T x V] buffer.  Everything allocated beyond the inputs and outputs is the two
+    # workspaces; the backward one is the [chunk x V] bf16 dZ block plus O(T) scalars, and
+    # below one bf16 logits copy whenever T > 256.
+    fws_b = flce.flce_forward_workspace_size(T, Hd, V)
+    bws_b = flce.flce_backward_workspace_size(T, Hd, V)
+    chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_b)
+    v_pad = (V + 63) // 64 * 64
+    assert bws_b <= 2 * chunk * v_pad + 4 * T + (1 << 20)
+    assert fws_b <= (8 * 16 + 4) * (T + 128) + (1 << 20)  # (m, s) per token and vocab range, at most 16 ranges
+    io = 2 * T * Hd + 2 * V * Hd + 8 * T + 4 * T + 3 * 4 * T + 8 + 2 * T * Hd + 4 * V * Hd
+    assert peak_extra <= io + fws_b + bws_b + (64 << 20)  # caching-allocator rounding
     if T > 256:
-        assert flce.flce_backward_workspace_size(T, Hd, V) < T * V * 2
-        assert peak_extra < T * V * 2 + 4 * V * Hd + 4 * T * Hd + 2 * V * Hd
+        assert bws_b < T * V * 2
     valid = inp.targets != inp.ignore_index
     assert int(out["n_valid"].item()) == int(valid.sum())
     rng = np.random.default_rng(123)
