@@ -243,7 +243,15 @@ def run_ours(args):
     out_b = {"dH": torch.empty((T, Hd), dtype=torch.bfloat16, device=dev),
              "dW": torch.empty((V, Hd), dtype=torch.float32, device=dev)}
     fws = torch.empty(flce.flce_forward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
-    bws = torch.empty(flce.flce_backward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
+    bws_bytes = flce.flce_backward_workspace_size(T, Hd, V)
+    if args.bwd_chunk:
+        # a workspace whose dZ block holds `bwd_chunk` token rows (the library sizes its chunk
+        # from the workspace it is given)
+        base_chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes)
+        bws_bytes += 2 * (args.bwd_chunk - base_chunk) * ((V + 63) // 64 * 64)
+        if flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes) != min(args.bwd_chunk, (T + 127) // 128 * 128):
+            raise SystemExit("--bwd-chunk must be a positive multiple of 128")
+    bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
 
     def step(Hx, Wx, yx, dlx):
         flce.flce_forward(Hx, Wx, yx, inp.ignore_index, wl.reduction, workspace=fws, out=out_f)
@@ -257,12 +265,16 @@ def run_ours(args):
     def max_over_ranks(x):
         return reduce_max(x, dev)
 
-    # Device memory across the warm-up steps: the library allocates nothing itself, so the
-    # driver's free-memory count must not move, and the caller's buffers are the inputs,
-    # the outputs and the two workspaces (the [chunk x V] dZ block being the largest).
+    # Device memory: the library allocates nothing itself.  The first step loads its module
+    # (kernels plus the 32 MiB static scratch of the workspace-free forward); after that the
+    # driver's free-memory count must not move, and the caller's buffers are the inputs, the
+    # outputs and the two workspaces (the [chunk x V] dZ block being the largest).
+    barrier()
+    free_before = torch.cuda.mem_get_info(dev)[0]
+    step(H, W, y, dloss)
     barrier()
     free0 = torch.cuda.mem_get_info(dev)[0]
-    for _ in range(args.warmup):
+    for _ in range(args.warmup - 1):
         step(H, W, y, dloss)
     barrier()
     free1 = torch.cuda.mem_get_info(dev)[0]
@@ -271,6 +283,7 @@ def run_ours(args):
     memory = {"logits_copy_bytes": T * V * 2, "workspace_bytes": int(fws.numel() + bws.numel()),
               "dz_block_bytes": 2 * chunk * ((V + 63) // 64 * 64), "io_bytes": int(io_bytes),
               "torch_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(dev)),
+              "module_load_bytes": int(free_before - free0),
               "driver_free_delta_over_warmup_bytes": int(free0 - free1)}
     for k in ("fwd", "bwd"):
         st = flce.flce_read_device_status(fws if k == "fwd" else bws)
@@ -442,6 +455,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of one step")
+    ap.add_argument("--bwd-chunk", type=int, default=0,
+                    help="backward token chunk (a multiple of 128; default: the library's default workspace)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

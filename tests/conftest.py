@@ -18,4 +18,7 @@ def cuda_device():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    return torch.device("cuda:0")
+    dev = torch.device("cuda:0")
+    torch.cuda.init()
+    torch.zeros(1, device=dev)  # a context and an allocator for the device before any test uses them
+    return dev
