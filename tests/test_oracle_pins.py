@@ -83,13 +83,16 @@ def pin_torch_library():
         out = torch.nn.functional.cross_entropy(
             torch.nn.functional.linear(Ht, Wt), yt, ignore_index=IGN, reduction=red)
         out.backward(torch.tensor(dloss) if red == "none" else torch.tensor(dloss[0]))
-        f = fo.forward(H, W, y, IGN, red)
-        assert np.allclose(np.asarray(f.loss), out.detach().numpy(), rtol=1e-13, atol=1e-13)
         lse_t = torch.logsumexp(torch.tensor(H) @ torch.tensor(W).T, dim=1).numpy()
-        assert np.allclose(f.lse, lse_t, rtol=1e-13, atol=1e-13)
-        dH, dW = fo.backward(dloss, H, W, y, IGN, red)
-        assert np.allclose(dH, Ht.grad.numpy(), rtol=1e-12, atol=1e-13)
-        assert np.allclose(dW, Wt.grad.numpy(), rtol=1e-12, atol=1e-13)
+        # one row block, and blocks of 4 rows (the last one ragged) to exercise the
+        # oracle's accumulation across row blocks
+        for rb in (256, 4):
+            f = fo.forward(H, W, y, IGN, red, row_block=rb)
+            assert np.allclose(np.asarray(f.loss), out.detach().numpy(), rtol=1e-13, atol=1e-13)
+            assert np.allclose(f.lse, lse_t, rtol=1e-13, atol=1e-13)
+            dH, dW = fo.backward(dloss, H, W, y, IGN, red, row_block=rb)
+            assert np.allclose(dH, Ht.grad.numpy(), rtol=1e-12, atol=1e-13)
+            assert np.allclose(dW, Wt.grad.numpy(), rtol=1e-12, atol=1e-13)
 
 
 def pin_finite_differences():
@@ -345,6 +348,23 @@ def test_target_out_of_range_is_an_error():
 
 # ----------------------------------------------------------------------------- planted mistakes
 
+def _backward_with(contract):
+    """The oracle's backward with its two contractions replaced by `contract`."""
+    def bwd(dloss, H, W, targets, ignore_index=-100, reduction="mean", row_block=256):
+        H = np.asarray(H, dtype=np.float64)
+        W = np.asarray(W, dtype=np.float64)
+        targets = np.asarray(targets, dtype=np.int64)
+        g = fo.upstream_grad(dloss, targets, W.shape[0], ignore_index, reduction)
+        dH, dW = np.zeros_like(H), np.zeros_like(W)
+        for r0 in range(0, H.shape[0], row_block):
+            r1 = min(H.shape[0], r0 + row_block)
+            Z = fo.logits(H[r0:r1], W)
+            dZ = fo._dZ(Z, fo._row_lse(Z), targets[r0:r1], g[r0:r1])
+            dW = contract(dZ, H[r0:r1], W, dH, r0, r1, dW)
+        return dH, dW
+    return bwd
+
+
 def _mutants():
     real_forward, real_dZ, real_logits, real_row_lse = fo.forward, fo._dZ, fo.logits, fo._row_lse
     real_upstream = fo.upstream_grad
@@ -387,6 +407,18 @@ def _mutants():
     def dz_scaled_twice(Z, lse, targets, g):
         return real_dZ(Z, lse, targets, g) * 2.0
 
+    def keeps_last_block(dZ, Hb, W, dH, r0, r1, dW):
+        dH[r0:r1] = dZ @ W
+        return dZ.T @ Hb                      # '=' where the sum needs '+='
+
+    def dW_rows_reversed(dZ, Hb, W, dH, r0, r1, dW):
+        dH[r0:r1] = dZ @ W
+        return dW + dZ.T @ Hb[::-1]           # token rows paired with the wrong dZ rows
+
+    def dH_vocab_reversed(dZ, Hb, W, dH, r0, r1, dW):
+        dH[r0:r1] = dZ @ W[::-1]              # vocab rows paired with the wrong dZ columns
+        return dW + dZ.T @ Hb
+
     return {
         "dZ drops the one-hot term": ("_dZ", dz_no_onehot),
         "dZ adds the one-hot term": ("_dZ", dz_wrong_sign),
@@ -397,6 +429,9 @@ def _mutants():
         "mean divides by T, not N": ("forward", forward_mean_over_T),
         "logp with the wrong sign": ("forward", forward_logp_sign),
         "ignored rows keep a gradient": ("upstream_grad", upstream_keeps_ignored),
+        "dW keeps only the last row block": ("backward", _backward_with(keeps_last_block)),
+        "dW pairs dZ with the wrong token rows": ("backward", _backward_with(dW_rows_reversed)),
+        "dH pairs dZ with the wrong vocab rows": ("backward", _backward_with(dH_vocab_reversed)),
     }
 
 
@@ -412,3 +447,14 @@ def test_planted_mistakes(name, monkeypatch):
         except (AssertionError, ValueError, FloatingPointError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake: {name}"
+
+
+def test_planted_mistake_harness_control(monkeypatch):
+    """The rebuilt backward used by the gradient mutants, given the right
+    contractions, passes every pin: the mutants are caught for their mistakes."""
+    def right(dZ, Hb, W, dH, r0, r1, dW):
+        dH[r0:r1] = dZ @ W
+        return dW + dZ.T @ Hb
+    monkeypatch.setattr(fo, "backward", _backward_with(right))
+    for pin in PINS:
+        pin()
