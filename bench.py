@@ -211,6 +211,176 @@ def run_reference(args):
     return 0
 
 
+class LossPath:
+    """The hot path: flce_forward + flce_backward (8·T·Hd·V FLOPs per step).  Inputs H, W,
+    targets, dloss; the loss and per-token logp are read back, dH and dW stay on the device."""
+
+    name = "loss"
+
+    def __init__(self, flce, torch, inp, wl, dev, args):
+        self.flce, self.torch, self.inp, self.wl, self.dev = flce, torch, inp, wl, dev
+        T, Hd, V = inp.T, inp.Hd, inp.V
+        self.metric = METRIC
+        self.flops_per_step = 8.0 * T * Hd * V
+        self.host = host_inputs(torch, inp, with_dloss=True)
+        self.ins = tuple(t.to(dev) for t in self.host)
+        self.fws = torch.empty(flce.flce_forward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
+        bws_bytes = flce.flce_backward_workspace_size(T, Hd, V)
+        if args.bwd_chunk:
+            # a workspace whose dZ block holds `bwd_chunk` token rows (the library sizes its
+            # chunk from the workspace it is given)
+            base_chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes)
+            bws_bytes += 2 * (args.bwd_chunk - base_chunk) * ((V + 63) // 64 * 64)
+            if flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes) != min(args.bwd_chunk, (T + 127) // 128 * 128):
+                raise SystemExit("--bwd-chunk must be a positive multiple of 128")
+        self.bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
+        self.chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes)
+        self.outs = self.new_outputs()
+
+    def new_outputs(self):
+        torch, T, Hd, V, dev = self.torch, self.inp.T, self.inp.Hd, self.inp.V, self.dev
+        return {"loss": torch.empty(T if self.wl.reduction == "none" else 1, dtype=torch.float32, device=dev),
+                "lse": torch.empty(T, dtype=torch.float32, device=dev),
+                "logp": torch.empty(T, dtype=torch.float32, device=dev),
+                "n_valid": torch.empty(1, dtype=torch.int64, device=dev),
+                "dH": torch.empty((T, Hd), dtype=torch.bfloat16, device=dev),
+                "dW": torch.empty((V, Hd), dtype=torch.float32, device=dev)}
+
+    def step(self, ins, outs):
+        H, W, y, dl = ins
+        f, ign, red = self.flce, self.inp.ignore_index, self.wl.reduction
+        f.flce_forward(H, W, y, ign, red, workspace=self.fws, out=outs)
+        f.flce_backward(dl, H, W, y, outs["lse"], ign, red, workspace=self.bws, out=outs)
+
+    def readback(self, outs):
+        return [outs["loss"], outs["logp"]]
+
+    def workspaces(self):
+        return [self.fws, self.bws]
+
+    def config(self):
+        return {"backward_chunk_tokens": self.chunk}
+
+    def dz_block_bytes(self):
+        return 2 * self.chunk * ((self.inp.V + 63) // 64 * 64)
+
+
+class ScorePath:
+    """flce_score: per-token logp, lse and greedy token, no loss and no backward
+    (2·T·Hd·V FLOPs per step).  Inputs H, W, targets; logp and the greedy token are read back."""
+
+    name = "score"
+
+    def __init__(self, flce, torch, inp, wl, dev, args):
+        self.flce, self.torch, self.inp, self.wl, self.dev = flce, torch, inp, wl, dev
+        T, Hd, V = inp.T, inp.Hd, inp.V
+        self.metric = "scoring tokens/s (per-token logp + lse + greedy token, no backward)"
+        self.flops_per_step = 2.0 * T * Hd * V
+        self.host = host_inputs(torch, inp, with_dloss=False)
+        self.ins = tuple(t.to(dev) for t in self.host)
+        lib = flce.load_library()
+        self.ws = torch.empty(max(lib.flce_score_workspace_size(T, Hd, V), 256), dtype=torch.uint8, device=dev)
+        self.outs = self.new_outputs()
+
+    def new_outputs(self):
+        torch, T, dev = self.torch, self.inp.T, self.dev
+        return {"logp": torch.empty(T, dtype=torch.float32, device=dev),
+                "lse": torch.empty(T, dtype=torch.float32, device=dev),
+                "argmax": torch.empty(T, dtype=torch.int64, device=dev)}
+
+    def step(self, ins, outs):
+        H, W, y = ins
+        self.flce.flce_score(H, W, y, self.inp.ignore_index, workspace=self.ws, out=outs)
+
+    def readback(self, outs):
+        return [outs["logp"], outs["argmax"]]
+
+    def workspaces(self):
+        return [self.ws]
+
+    def config(self):
+        return {}
+
+    def dz_block_bytes(self):
+        return 0
+
+
+class VocabSplitPath:
+    """The vocab-parallel split emulated on one GPU: W's rows cut into `n` equal shards,
+    flce_forward_shard per shard, flce_combine_shards, flce_backward_shard per shard
+    (8·T·Hd·V FLOPs per step).  Each shard's bf16 dH partial is left for the caller's
+    all-reduce, which is not part of the op; inputs and read-back as the loss path."""
+
+    name = "vocab-split"
+
+    def __init__(self, flce, torch, inp, wl, dev, args):
+        self.flce, self.torch, self.inp, self.wl, self.dev = flce, torch, inp, wl, dev
+        T, Hd, V = inp.T, inp.Hd, inp.V
+        n = args.shards
+        if n < 1 or V % n:
+            raise SystemExit(f"--shards {n} must divide V = {V}")
+        self.bounds = [(i * V // n, (i + 1) * V // n) for i in range(n)]
+        self.metric = f"fused linear-CE fwd+bwd tokens/s, vocab split over {n} emulated ranks"
+        self.flops_per_step = 8.0 * T * Hd * V
+        self.host = host_inputs(torch, inp, with_dloss=True)
+        self.ins = tuple(t.to(dev) for t in self.host)
+        lib = flce.load_library()
+        Vs = V // n
+        self.fws = torch.empty(flce.flce_forward_workspace_size(T, Hd, Vs), dtype=torch.uint8, device=dev)
+        self.cws = torch.empty(max(lib.flce_combine_workspace_size(T, n), 256), dtype=torch.uint8, device=dev)
+        self.bws = torch.empty(flce.flce_backward_workspace_size(T, Hd, Vs), dtype=torch.uint8, device=dev)
+        self.chunk = flce.flce_backward_chunk_tokens(T, Hd, Vs, self.bws.numel())
+        self.outs = self.new_outputs()
+
+    def new_outputs(self):
+        torch, T, Hd, V, dev = self.torch, self.inp.T, self.inp.Hd, self.inp.V, self.dev
+        n = len(self.bounds)
+        return {"shard_lse": torch.empty((n, T), dtype=torch.float32, device=dev),
+                "shard_zy": torch.empty((n, T), dtype=torch.float32, device=dev),
+                "loss": torch.empty(T if self.wl.reduction == "none" else 1, dtype=torch.float32, device=dev),
+                "lse": torch.empty(T, dtype=torch.float32, device=dev),
+                "logp": torch.empty(T, dtype=torch.float32, device=dev),
+                "n_valid": torch.empty(1, dtype=torch.int64, device=dev),
+                "dH_partials": torch.empty((n, T, Hd), dtype=torch.bfloat16, device=dev),
+                "dW": torch.empty((V, Hd), dtype=torch.float32, device=dev)}
+
+    def step(self, ins, outs):
+        H, W, y, dl = ins
+        f, ign, red, V = self.flce, self.inp.ignore_index, self.wl.reduction, self.inp.V
+        for i, (a, b) in enumerate(self.bounds):
+            f.flce_forward_shard(H, W[a:b], y, a, V, ign, workspace=self.fws,
+                                 out={"shard_lse": outs["shard_lse"][i], "shard_zy": outs["shard_zy"][i]})
+        f.flce_combine_shards(outs["shard_lse"], outs["shard_zy"], y, V, ign, red, workspace=self.cws, out=outs)
+        for i, (a, b) in enumerate(self.bounds):
+            f.flce_backward_shard(dl, H, W[a:b], y, outs["lse"], a, V, ign, red, workspace=self.bws,
+                                  out={"dH": outs["dH_partials"][i], "dW": outs["dW"][a:b]})
+
+    def readback(self, outs):
+        return [outs["loss"], outs["logp"]]
+
+    def workspaces(self):
+        return [self.fws, self.cws, self.bws]
+
+    def config(self):
+        return {"vocab_shards": len(self.bounds), "shard_rows": self.bounds[0][1] - self.bounds[0][0],
+                "backward_chunk_tokens": self.chunk}
+
+    def dz_block_bytes(self):
+        return 2 * self.chunk * ((self.bounds[0][1] - self.bounds[0][0] + 63) // 64 * 64)
+
+
+PATHS = {"loss": LossPath, "score": ScorePath, "vocab-split": VocabSplitPath}
+
+
+def host_inputs(torch, inp, with_dloss):
+    H_h = torch.from_numpy(inp.H_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_h = torch.from_numpy(inp.W_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_h = torch.from_numpy(inp.targets).pin_memory()
+    if not with_dloss:
+        return (H_h, W_h, y_h)
+    return (H_h, W_h, y_h, torch.from_numpy(inp.dloss).pin_memory())
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -227,35 +397,10 @@ def run_ours(args):
     inp = generate(wl, seed=rank, T=args.T, Hd=args.Hd, V=args.V)
     T, Hd, V = inp.T, inp.Hd, inp.V
     stream = torch.cuda.current_stream(dev)
+    path = PATHS[args.path](flce, torch, inp, wl, dev, args)
 
-    H_h = torch.from_numpy(inp.H_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    W_h = torch.from_numpy(inp.W_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    y_h = torch.from_numpy(inp.targets).pin_memory()
-    dl_h = torch.from_numpy(inp.dloss).pin_memory()
-    H = H_h.to(dev)
-    W = W_h.to(dev)
-    y = y_h.to(dev)
-    dloss = dl_h.to(dev)
-    out_f = {"loss": torch.empty(T if wl.reduction == "none" else 1, dtype=torch.float32, device=dev),
-             "lse": torch.empty(T, dtype=torch.float32, device=dev),
-             "logp": torch.empty(T, dtype=torch.float32, device=dev),
-             "n_valid": torch.empty(1, dtype=torch.int64, device=dev)}
-    out_b = {"dH": torch.empty((T, Hd), dtype=torch.bfloat16, device=dev),
-             "dW": torch.empty((V, Hd), dtype=torch.float32, device=dev)}
-    fws = torch.empty(flce.flce_forward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
-    bws_bytes = flce.flce_backward_workspace_size(T, Hd, V)
-    if args.bwd_chunk:
-        # a workspace whose dZ block holds `bwd_chunk` token rows (the library sizes its chunk
-        # from the workspace it is given)
-        base_chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes)
-        bws_bytes += 2 * (args.bwd_chunk - base_chunk) * ((V + 63) // 64 * 64)
-        if flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes) != min(args.bwd_chunk, (T + 127) // 128 * 128):
-            raise SystemExit("--bwd-chunk must be a positive multiple of 128")
-    bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
-
-    def step(Hx, Wx, yx, dlx):
-        flce.flce_forward(Hx, Wx, yx, inp.ignore_index, wl.reduction, workspace=fws, out=out_f)
-        flce.flce_backward(dlx, Hx, Wx, yx, out_f["lse"], inp.ignore_index, wl.reduction, workspace=bws, out=out_b)
+    def step():
+        path.step(path.ins, path.outs)
 
     def barrier():
         if world > 1:
@@ -268,27 +413,27 @@ def run_ours(args):
     # Device memory: the library allocates nothing itself.  The first step loads its module
     # (kernels plus the 32 MiB static scratch of the workspace-free forward); after that the
     # driver's free-memory count must not move, and the caller's buffers are the inputs, the
-    # outputs and the two workspaces (the [chunk x V] dZ block being the largest).
+    # outputs and the workspaces (the [chunk x V] dZ block being the largest).
     barrier()
     free_before = torch.cuda.mem_get_info(dev)[0]
-    step(H, W, y, dloss)
+    step()
     barrier()
     free0 = torch.cuda.mem_get_info(dev)[0]
     for _ in range(args.warmup - 1):
-        step(H, W, y, dloss)
+        step()
     barrier()
     free1 = torch.cuda.mem_get_info(dev)[0]
-    chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws.numel())
-    io_bytes = sum(t.numel() * t.element_size() for t in (H, W, y, dloss, *out_f.values(), *out_b.values()))
-    memory = {"logits_copy_bytes": T * V * 2, "workspace_bytes": int(fws.numel() + bws.numel()),
-              "dz_block_bytes": 2 * chunk * ((V + 63) // 64 * 64), "io_bytes": int(io_bytes),
+    io_bytes = sum(t.numel() * t.element_size() for t in (*path.ins, *path.outs.values()))
+    memory = {"logits_copy_bytes": T * V * 2,
+              "workspace_bytes": int(sum(w.numel() for w in path.workspaces())),
+              "dz_block_bytes": int(path.dz_block_bytes()), "io_bytes": int(io_bytes),
               "torch_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(dev)),
               "module_load_bytes": int(free_before - free0),
               "driver_free_delta_over_warmup_bytes": int(free0 - free1)}
-    for k in ("fwd", "bwd"):
-        st = flce.flce_read_device_status(fws if k == "fwd" else bws)
+    for ws in path.workspaces():
+        st = flce.flce_read_device_status(ws)
         if st != 0:
-            raise RuntimeError(f"device status {st} after the warm-up {k}")
+            raise RuntimeError(f"device status {st} after the warm-up")
 
     # ---- device-resident timed region (value); per-kernel events for the roofline.
     # With --graph the step is captured once into a CUDA graph and the timed loop
@@ -301,7 +446,7 @@ def run_ours(args):
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
             with torch.cuda.graph(graph, stream=cap):
-                step(H, W, y, dloss)
+                step()
         stream.wait_stream(cap)
         for _ in range(args.warmup):
             graph.replay()
@@ -317,14 +462,14 @@ def run_ours(args):
             if graph is not None:
                 graph.replay()
             else:
-                step(H, W, y, dloss)
+                step()
         ev1.record(stream)
         barrier()
     flce.flce_profile_enable(False)
     if graph is not None:
         flce.flce_profile_enable(True)
         for _ in range(args.steps):
-            step(H, W, y, dloss)
+            step()
         flce.flce_profile_enable(False)
     kstats = flce.flce_profile_collect()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1))
@@ -333,26 +478,25 @@ def run_ours(args):
     gpu_launches = sum(v["launches"] for v in kstats.values())
 
     # ---- end to end through the public API with host buffers.  Every step copies its
-    # inputs (H, W, targets, dloss) in from pinned host memory and reads its result --
-    # the loss and the per-token log p(target) -- back out; dH and dW stay on the device,
-    # where the rest of a training step consumes them.  The copies run on two copy
-    # streams (one per direction) and overlap the neighbouring steps' compute through
-    # double-buffered device inputs and outputs.
+    # inputs (H, W, targets and, with a backward, dloss) in from pinned host memory and
+    # reads its result back out (the loss and per-token log p(target); for scoring, log p
+    # and the greedy token); gradients stay on the device, where the rest of a training
+    # step consumes them.  The copies run on two copy streams (one per direction) and
+    # overlap the neighbouring steps' compute through double-buffered device inputs and
+    # outputs.
     e2e_steps = max(2, args.steps)
-    logp_h = torch.empty(T, dtype=torch.float32).pin_memory()
-    loss_h = torch.empty_like(out_f["loss"], device="cpu").pin_memory()
+    back_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in path.readback(path.outs)]
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
-    ins = [(H, W, y, dloss), tuple(torch.empty_like(t) for t in (H, W, y, dloss))]
-    outs = [(out_f, out_b), ({k: torch.empty_like(v) for k, v in out_f.items()},
-                             {k: torch.empty_like(v) for k, v in out_b.items()})]
+    ins = [path.ins, tuple(torch.empty_like(t) for t in path.ins)]
+    outs = [path.outs, path.new_outputs()]
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def h2d(j):
         with torch.cuda.stream(s_in):
-            for dst, src in zip(ins[j], (H_h, W_h, y_h, dl_h)):
+            for dst, src in zip(ins[j], path.host):
                 dst.copy_(src, non_blocking=True)
             ev_in[j].record(s_in)
 
@@ -372,25 +516,22 @@ def run_ours(args):
         stream.wait_event(ev_in[j])
         if i >= 2:
             stream.wait_event(ev_out[j])  # that output set was last copied out after step i - 2
-        Hx, Wx, yx, dx = ins[j]
-        of, ob = outs[j]
-        flce.flce_forward(Hx, Wx, yx, inp.ignore_index, wl.reduction, workspace=fws, out=of, stream=stream)
-        flce.flce_backward(dx, Hx, Wx, yx, of["lse"], inp.ignore_index, wl.reduction, workspace=bws, out=ob,
-                           stream=stream)
+        with torch.cuda.stream(stream):
+            path.step(ins[j], outs[j])
         ev_comp[j].record(stream)
         s_out.wait_event(ev_comp[j])
         with torch.cuda.stream(s_out):
-            loss_h.copy_(of["loss"], non_blocking=True)
-            logp_h.copy_(of["logp"], non_blocking=True)
+            for dst, src in zip(back_h, path.readback(outs[j])):
+                dst.copy_(src, non_blocking=True)
             ev_out[j].record(s_out)
     stream.wait_event(ev_out[(e2e_steps - 1) % 2])
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    h2d = H_h.numel() * 2 + W_h.numel() * 2 + y_h.numel() * 8 + dl_h.numel() * 4
-    d2h = loss_h.numel() * 4 + logp_h.numel() * 4
+    h2d_bytes = sum(t.numel() * t.element_size() for t in path.host)
+    d2h_bytes = sum(t.numel() * t.element_size() for t in back_h)
     e2e = {"value": whole_job_tokens_per_s(T * e2e_steps, world, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+           "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "steps": e2e_steps}
 
     if rank != 0:
         if world > 1:
@@ -398,31 +539,33 @@ def run_ours(args):
         return 0
 
     peaks, peak_src = load_peaks()
-    tflops = world * 8.0 * T * Hd * V * args.steps / (ms_total / 1000.0) / 1e12
+    tflops = world * path.flops_per_step * args.steps / (ms_total / 1000.0) / 1e12
     dom_name, dom = max(kstats.items(), key=lambda kv: kv[1]["total_ms"])
     avg_ms = dom["total_ms"] / dom["launches"]
     ach = (dom["flops"] / dom["launches"]) / (avg_ms / 1000.0) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    traffic = traffic_from_profiles(dom_name)
+    traffic = traffic_from_profiles(dom_name) if args.path == "loss" else None
     kernels = {k: {"launches": v["launches"], "avg_ms": v["total_ms"] / v["launches"],
                    "share": v["total_ms"] / sum(x["total_ms"] for x in kstats.values()),
                    "tflops": (v["flops"] / (v["total_ms"] / 1000.0) / 1e12) if v["flops"] else None}
                for k, v in sorted(kstats.items())}
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name if (T, Hd, V) == (wl.T, wl.Hd, wl.V) else f"{wl.name} at T={T} Hd={Hd} V={V}",
-                   "T": T, "Hd": Hd, "V": V, "reduction": wl.reduction,
-                   "backward_chunk_tokens": chunk,
-                   "l2": "inputs larger than L2 (H %.0f MB + W %.0f MB > 129 MB), no flush" % (
+    config = {"workload": wl.name if (T, Hd, V) == (wl.T, wl.Hd, wl.V) else f"{wl.name} at T={T} Hd={Hd} V={V}",
+              "T": T, "Hd": Hd, "V": V, "reduction": wl.reduction}
+    if args.path != "loss":
+        config["path"] = args.path
+    config.update(path.config())
+    config.update({"l2": "inputs larger than L2 (H %.0f MB + W %.0f MB > 129 MB), no flush" % (
                        T * Hd * 2 / 1e6, V * Hd * 2 / 1e6),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "launch": "cuda graph replay" if args.graph else "eager"},
+                   "launch": "cuda graph replay" if args.graph else "eager"})
+    line = {
+        "metric": path.metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config,
         "tflops": tflops,
         "frac_of_bf16_peak": {"burst": tflops / float(peaks.get("bf16_tflops", 1)),
                               "sustained": tflops / peak, "source": peak_src},
-        "model_tflops_6THV": tflops * 6.0 / 8.0,
         "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                      "frac": ach / peak, "traffic": traffic,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})",
@@ -433,6 +576,8 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "memory": memory,
     }
+    if args.path == "loss":
+        line["model_tflops_6THV"] = tflops * 6.0 / 8.0
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(inp, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -455,6 +600,10 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of one step")
+    ap.add_argument("--path", choices=sorted(PATHS), default="loss",
+                    help="loss: flce_forward + flce_backward (the default); score: flce_score alone; "
+                         "vocab-split: the shard entry points over --shards equal vocab shards")
+    ap.add_argument("--shards", type=int, default=2, help="vocab shards of --path vocab-split")
     ap.add_argument("--bwd-chunk", type=int, default=0,
                     help="backward token chunk (a multiple of 128; default: the library's default workspace)")
     args = ap.parse_args()

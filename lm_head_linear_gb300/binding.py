@@ -123,6 +123,15 @@ def _check_inputs(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor):
         raise ValueError(f"shape mismatch: H {tuple(H.shape)}, W {tuple(W.shape)}, targets {tuple(targets.shape)}")
     if not (H.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
         raise ValueError("H, W and targets must be contiguous")
+    if not (H.device == W.device == targets.device):
+        raise ValueError("H, W and targets must be on one device")
+
+
+def _check_rows(name: str, t: torch.Tensor, shape, dtype, device):
+    """A device array the library reads through its pointer: same device, dtype, shape."""
+    if t.device != device or t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a {dtype} tensor of shape {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
 
 
 def flce_forward_workspace_size(T: int, Hd: int, V: int) -> int:
@@ -140,7 +149,22 @@ def flce_backward_chunk_tokens(T: int, Hd: int, V: int, workspace_bytes: int) ->
 def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
     if workspace is None:
         return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if workspace.device != device or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError(f"the workspace must be a contiguous uint8 tensor on {device}")
     return workspace
+
+
+def _out(out: Optional[dict], key: str, shape, dtype, device) -> torch.Tensor:
+    """out[key] if the caller gave one (checked: the library writes through its pointer),
+    else a new tensor."""
+    t = (out or {}).get(key)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    want = (shape,) if isinstance(shape, int) else tuple(shape)
+    if tuple(t.shape) != want or t.dtype != dtype or t.device != device or not t.is_contiguous():
+        raise ValueError(f"out[{key!r}] must be a contiguous {dtype} tensor of shape {want} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    return t
 
 
 def flce_forward(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
@@ -158,19 +182,10 @@ def flce_forward(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore
     V = W.shape[0]
     red = REDUCTIONS[reduction]
     dev = H.device
-    out = out or {}
-    loss = out.get("loss")
-    if loss is None:
-        loss = torch.empty(T if red == 0 else 1, dtype=torch.float32, device=dev)
-    lse = out.get("lse")
-    if lse is None:
-        lse = torch.empty(T, dtype=torch.float32, device=dev)
-    logp = out.get("logp")
-    if logp is None:
-        logp = torch.empty(T, dtype=torch.float32, device=dev)
-    n_valid = out.get("n_valid")
-    if n_valid is None:
-        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    loss = _out(out, "loss", T if red == 0 else 1, torch.float32, dev)
+    lse = _out(out, "lse", T, torch.float32, dev)
+    logp = _out(out, "logp", T, torch.float32, dev)
+    n_valid = _out(out, "n_valid", 1, torch.int64, dev)
     need = lib.flce_forward_workspace_size(T, Hd, V)
     ws = _workspace(need, dev, workspace)
     st = lib.flce_forward(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), red, _ptr(loss), _ptr(lse),
@@ -202,14 +217,10 @@ def flce_backward(dloss: Optional[torch.Tensor], H: torch.Tensor, W: torch.Tenso
         dlogp = dlogp.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
         if dlogp.numel() != T:
             raise ValueError("dlogp must have T elements")
+    _check_rows("lse", lse, (T,), torch.float32, dev)
     lse = lse.contiguous()
-    out = out or {}
-    dH = out.get("dH")
-    if dH is None:
-        dH = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
-    dW = out.get("dW")
-    if dW is None:
-        dW = torch.empty((V, Hd), dtype=torch.float32, device=dev)
+    dH = _out(out, "dH", (T, Hd), torch.bfloat16, dev)
+    dW = _out(out, "dW", (V, Hd), torch.float32, dev)
     need = lib.flce_backward_workspace_size(T, Hd, V)
     ws = _workspace(need, dev, workspace)
     if dlogp is None:
@@ -223,17 +234,20 @@ def flce_backward(dloss: Optional[torch.Tensor], H: torch.Tensor, W: torch.Tenso
     return dH, dW, ws
 
 
+
+
 def flce_score(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
-               workspace: Optional[torch.Tensor] = None, stream=None):
-    """Run ``flce_score``; returns ``(logp [T] fp32, lse [T] fp32, argmax [T] int64, workspace)``."""
+               workspace: Optional[torch.Tensor] = None, stream=None, out: Optional[dict] = None):
+    """Run ``flce_score``; returns ``(logp [T] fp32, lse [T] fp32, argmax [T] int64, workspace)``.
+    ``out`` may hold preallocated ``logp``, ``lse`` and ``argmax`` tensors."""
     _check_inputs(H, W, targets)
     lib = load_library()
     T, Hd = H.shape
     V = W.shape[0]
     dev = H.device
-    logp = torch.empty(T, dtype=torch.float32, device=dev)
-    lse = torch.empty(T, dtype=torch.float32, device=dev)
-    argmax = torch.empty(T, dtype=torch.int64, device=dev)
+    logp = _out(out, "logp", T, torch.float32, dev)
+    lse = _out(out, "lse", T, torch.float32, dev)
+    argmax = _out(out, "argmax", T, torch.int64, dev)
     ws = _workspace(lib.flce_score_workspace_size(T, Hd, V), dev, workspace)
     _check(lib.flce_score(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), _ptr(logp), _ptr(lse),
                           _ptr(argmax), _ptr(ws), ws.numel(), _stream_handle(stream)))
@@ -241,15 +255,17 @@ def flce_score(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_i
 
 
 def flce_forward_shard(H: torch.Tensor, W_shard: torch.Tensor, targets: torch.Tensor, vocab_offset: int,
-                       V_total: int, ignore_index: int = -100, workspace: Optional[torch.Tensor] = None, stream=None):
-    """Run ``flce_forward_shard``; returns ``(shard_lse [T], shard_zy [T], workspace)``."""
+                       V_total: int, ignore_index: int = -100, workspace: Optional[torch.Tensor] = None, stream=None,
+                       out: Optional[dict] = None):
+    """Run ``flce_forward_shard``; returns ``(shard_lse [T], shard_zy [T], workspace)``.
+    ``out`` may hold preallocated ``shard_lse`` and ``shard_zy`` tensors."""
     _check_inputs(H, W_shard, targets)
     lib = load_library()
     T, Hd = H.shape
     Vs = W_shard.shape[0]
     dev = H.device
-    shard_lse = torch.empty(T, dtype=torch.float32, device=dev)
-    shard_zy = torch.empty(T, dtype=torch.float32, device=dev)
+    shard_lse = _out(out, "shard_lse", T, torch.float32, dev)
+    shard_zy = _out(out, "shard_zy", T, torch.float32, dev)
     ws = _workspace(lib.flce_forward_workspace_size(T, Hd, Vs), dev, workspace)
     _check(lib.flce_forward_shard(_ptr(H), _ptr(W_shard), _ptr(targets), T, Hd, Vs, int(vocab_offset), int(V_total),
                                   int(ignore_index), _ptr(shard_lse), _ptr(shard_zy), _ptr(ws), ws.numel(),
@@ -259,20 +275,25 @@ def flce_forward_shard(H: torch.Tensor, W_shard: torch.Tensor, targets: torch.Te
 
 def flce_combine_shards(shard_lse: torch.Tensor, shard_zy: torch.Tensor, targets: torch.Tensor, V_total: int,
                         ignore_index: int = -100, reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
-                        stream=None):
-    """Run ``flce_combine_shards`` on [n_shards, T] partials; returns ``(loss, lse, logp, n_valid, workspace)``."""
+                        stream=None, out: Optional[dict] = None):
+    """Run ``flce_combine_shards`` on [n_shards, T] partials; returns ``(loss, lse, logp, n_valid, workspace)``.
+    ``out`` may hold preallocated ``loss``, ``lse``, ``logp`` and ``n_valid`` tensors."""
     lib = load_library()
+    if shard_lse.dim() != 2 or not shard_lse.is_cuda:
+        raise ValueError("shard_lse must be a CUDA tensor [n_shards, T]")
     n_shards, T = shard_lse.shape
-    if shard_zy.shape != shard_lse.shape or targets.shape != (T,):
-        raise ValueError("shard_lse, shard_zy [n_shards, T] and targets [T]")
+    dev = shard_lse.device
+    _check_rows("shard_lse", shard_lse, (n_shards, T), torch.float32, dev)
+    _check_rows("shard_zy", shard_zy, (n_shards, T), torch.float32, dev)
+    _check_rows("targets", targets, (T,), torch.int64, dev)
     shard_lse = shard_lse.contiguous()
     shard_zy = shard_zy.contiguous()
+    targets = targets.contiguous()
     red = REDUCTIONS[reduction]
-    dev = shard_lse.device
-    loss = torch.empty(T if red == 0 else 1, dtype=torch.float32, device=dev)
-    lse = torch.empty(T, dtype=torch.float32, device=dev)
-    logp = torch.empty(T, dtype=torch.float32, device=dev)
-    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    loss = _out(out, "loss", T if red == 0 else 1, torch.float32, dev)
+    lse = _out(out, "lse", T, torch.float32, dev)
+    logp = _out(out, "logp", T, torch.float32, dev)
+    n_valid = _out(out, "n_valid", 1, torch.int64, dev)
     ws = _workspace(lib.flce_combine_workspace_size(T, n_shards), dev, workspace)
     _check(lib.flce_combine_shards(_ptr(shard_lse), _ptr(shard_zy), n_shards, _ptr(targets), T, int(V_total),
                                    int(ignore_index), red, _ptr(loss), _ptr(lse), _ptr(logp), _ptr(n_valid),
@@ -282,8 +303,10 @@ def flce_combine_shards(shard_lse: torch.Tensor, shard_zy: torch.Tensor, targets
 
 def flce_backward_shard(dloss: torch.Tensor, H: torch.Tensor, W_shard: torch.Tensor, targets: torch.Tensor,
                         lse: torch.Tensor, vocab_offset: int, V_total: int, ignore_index: int = -100,
-                        reduction: str = "mean", workspace: Optional[torch.Tensor] = None, stream=None):
-    """Run ``flce_backward_shard``; returns ``(dH_partial bf16 [T, Hd], dW_shard fp32 [V_shard, Hd], workspace)``."""
+                        reduction: str = "mean", workspace: Optional[torch.Tensor] = None, stream=None,
+                        out: Optional[dict] = None):
+    """Run ``flce_backward_shard``; returns ``(dH_partial bf16 [T, Hd], dW_shard fp32 [V_shard, Hd], workspace)``.
+    ``out`` may hold preallocated ``dH`` and ``dW`` tensors."""
     _check_inputs(H, W_shard, targets)
     lib = load_library()
     T, Hd = H.shape
@@ -293,8 +316,9 @@ def flce_backward_shard(dloss: torch.Tensor, H: torch.Tensor, W_shard: torch.Ten
     dloss = dloss.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
     if dloss.numel() != (T if red == 0 else 1):
         raise ValueError("dloss must have one element (mean / sum) or T elements (none)")
-    dH = torch.empty((T, Hd), dtype=torch.bfloat16, device=dev)
-    dW = torch.empty((Vs, Hd), dtype=torch.float32, device=dev)
+    _check_rows("lse", lse, (T,), torch.float32, dev)
+    dH = _out(out, "dH", (T, Hd), torch.bfloat16, dev)
+    dW = _out(out, "dW", (Vs, Hd), torch.float32, dev)
     ws = _workspace(lib.flce_backward_workspace_size(T, Hd, Vs), dev, workspace)
     _check(lib.flce_backward_shard(_ptr(dloss), _ptr(H), _ptr(W_shard), _ptr(targets), _ptr(lse.contiguous()), T, Hd,
                                    Vs, int(vocab_offset), int(V_total), int(ignore_index), red, _ptr(dH), _ptr(dW),

@@ -152,6 +152,30 @@ def test_argument_errors(cuda_device):
     assert e.value.status == 4
 
 
+def test_binding_rejects_buffers_the_library_cannot_use(cuda_device):
+    """Buffers the library would write or read through a raw pointer are checked in the
+    binding first: a host workspace, an output of the wrong shape or dtype, a host lse."""
+    inp = generate("tiny", T=64, Hd=64, V=100)
+    H, W, y, dl = to_device(inp, cuda_device)
+    with pytest.raises(ValueError):
+        flce.flce_forward(H, W, y, workspace=torch.empty(1 << 20, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        flce.flce_forward(H, W, y, out={"lse": torch.empty(63, device=cuda_device)})
+    with pytest.raises(ValueError):
+        flce.flce_forward(H, W, y, out={"n_valid": torch.empty(1, dtype=torch.int32, device=cuda_device)})
+    _, lse, _, _, _ = flce.flce_forward(H, W, y)
+    with pytest.raises(ValueError):
+        flce.flce_backward(dl, H, W, y, lse.cpu())
+    with pytest.raises(ValueError):
+        flce.flce_backward(dl, H, W, y, lse, out={"dW": torch.empty((100, 64), dtype=torch.bfloat16,
+                                                                      device=cuda_device)})
+    with pytest.raises(ValueError):
+        flce.flce_score(H, W, y, out={"argmax": torch.empty(64, dtype=torch.int32, device=cuda_device)})
+    with pytest.raises(ValueError):
+        flce.flce_combine_shards(torch.zeros((2, 64), device=cuda_device), torch.zeros((2, 64)), y, 100)
+    torch.cuda.synchronize()
+
+
 def test_autograd_wrapper(cuda_device):
     inp = generate("medium", T=300, Hd=128, V=2000)
     H, W, y, _ = to_device(inp, cuda_device)
