@@ -33,7 +33,8 @@
  *     whose target is out of range are treated as ignored.
  *   - H and W are bf16, row-major: H [T, Hd], W [V, Hd], each row contiguous.
  *     Hd must be a positive multiple of 64; H, W, dH and dW must be 16-byte
- *     aligned; the workspace 256-byte aligned.  T may be 0.  V >= 1.
+ *     aligned; the workspace 256-byte aligned; every other array aligned to
+ *     its element type (4 bytes for float, 8 for int64_t).  T may be 0.  V >= 1.
  *     T, V < 2^30.
  *   - Rows whose target equals ignore_index contribute zero loss and zero
  *     gradient and are not counted in n_valid.  ignore_index must lie outside
@@ -65,7 +66,8 @@ typedef enum flce_status {
   FLCE_OK = 0,
   FLCE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad reduction, ignore_index in [0, V) */
   FLCE_ERR_UNSUPPORTED = 2,  /* Hd not a multiple of 64, or the device is not sm_103 */
-  FLCE_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned (workspace: 256) */
+  FLCE_ERR_ALIGNMENT = 3,    /* H, W, dH, dW not 16-byte aligned, the workspace not 256-byte, or a
+                                per-token array not aligned to its element type */
   FLCE_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
   FLCE_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed; see flce_last_error() */
   FLCE_ERR_TARGET_RANGE = 6, /* device status: a target outside [0, V) and != ignore_index */
@@ -247,8 +249,13 @@ FLCE_API const char* flce_last_error(void);
 /* FLCE_ABI_VERSION of the loaded library. */
 FLCE_API int32_t flce_abi_version(void);
 
-/* Limit, in nanoseconds, of every bounded wait inside the kernels (default
- * 4e9).  Values below 1e6 are raised to 1e6.  Affects later launches only. */
+/* Limit, in nanoseconds, of every bounded wait inside the kernels.  Values
+ * below 1e6 are raised to 1e6.  Affects later launches only.  Until this is
+ * called the limit of each launch is max(4e9, 16 x K) ns, K being the longest
+ * contraction of one output tile in that launch (Hd in the forward and dZ
+ * kernels; V for dH tiles and the token chunk for dW tiles), since the longest
+ * wait spans one tile's K loop (about 8 SM-pair clocks per unit of K); once it
+ * is called, the given value is used for every launch. */
 FLCE_API void flce_set_wait_timeout_ns(uint64_t ns);
 
 /* ---- per-kernel timing, a profiling aid ------------------------------------

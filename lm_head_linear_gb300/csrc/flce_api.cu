@@ -6,6 +6,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -42,9 +43,29 @@ constexpr int32_t kMaxShards = 64;    // vocab shards one combine call merges
 // T and V bound: tile coordinates (block * 128 + row) stay inside int32 with room to spare.
 constexpr int64_t kMaxRows = int64_t(1) << 30;
 
-uint64_t g_timeout_ns = 4000000000ull;
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<bool> g_timeout_fixed{false};  // set by flce_set_wait_timeout_ns
+
+// Limit of the bounded waits of one GEMM launch whose longest tile has a K loop of
+// `k_max`.  The longest wait inside the kernels is the epilogue's wait for one
+// tile's whole K loop: a 256 x 256 pair tile needs 8 SM-pair clocks per unit of K
+// (131,072 FLOP at 16,384 dense bf16 FLOP per pair per clock), so 16 ns per unit of
+// K covers it twice over at 1 GHz.  A limit the caller fixed is used as it is.
+uint64_t wait_limit_ns(int64_t k_max) {
+  const uint64_t base = g_timeout_ns.load();
+  if (g_timeout_fixed.load()) return base;
+  return std::max<uint64_t>(base, 16ull * static_cast<uint64_t>(std::max<int64_t>(k_max, 0)));
+}
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The kernels read and write the per-token arrays with plain typed loads and
+// stores, so each pointer must carry its type's natural alignment (checked on the
+// host: a misaligned access would fault the device instead of returning an error).
+template <typename E>
+bool misaligned(const E* p) {
+  return (reinterpret_cast<uintptr_t>(p) % alignof(E)) != 0;
+}
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------------ device info
@@ -294,6 +315,7 @@ flce_status check_common(const void* H, const void* W, const int64_t* targets, i
   if (T > 0 && (!H || !targets)) return fail(FLCE_ERR_INVALID_ARG, "H or targets is NULL");
   if ((reinterpret_cast<uintptr_t>(H) | reinterpret_cast<uintptr_t>(W)) & 15)
     return fail(FLCE_ERR_ALIGNMENT, "H and W must be 16-byte aligned");
+  if (misaligned(targets)) return fail(FLCE_ERR_ALIGNMENT, "targets must be 8-byte aligned");
   return FLCE_OK;
 }
 
@@ -360,7 +382,7 @@ flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, co
   p.best_val = best_val;
   p.best_idx = best_idx;
   p.status = reinterpret_cast<int32_t*>(ws);
-  p.timeout_ns = g_timeout_ns;
+  p.timeout_ns = wait_limit_ns(Hd);
   const bool score = best_val != nullptr;
   const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[score ? MODE_SCORE : MODE_FWD], p.num_units));
   KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, 2.0 * T * Hd * V,
@@ -433,6 +455,8 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     return fail(FLCE_ERR_INVALID_ARG, "dloss (or dlogp), lse, dH or dW is NULL");
   if ((reinterpret_cast<uintptr_t>(dH) | reinterpret_cast<uintptr_t>(dW)) & 15)
     return fail(FLCE_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
+  if (misaligned(dloss) || misaligned(dlogp) || misaligned(lse))
+    return fail(FLCE_ERR_ALIGNMENT, "dloss, dlogp and lse must be 4-byte aligned");
   if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(workspace) & 255)
     return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
@@ -500,7 +524,7 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     p.lse = lse;
     p.g = g;
     p.status = status;
-    p.timeout_ns = g_timeout_ns;
+    p.timeout_ns = wait_limit_ns(Hd);
     p.n_split = 1;
 
     // (1) recomputed logit tiles -> dZ chunk
@@ -534,6 +558,7 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
     p.reduce_out = c > 0 ? 1 : 0;
     p.tile_counter = counters + c;
+    p.timeout_ns = wait_limit_ns(std::max<int64_t>(V, rows));  // dH tiles: K = V; dW tiles: K = rows
     {
       const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DHW], p.n_dh_tiles + p.n_dw_tiles));
       KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 4.0 * rows * Hd * V,
@@ -569,7 +594,10 @@ const char* flce_status_string(int32_t st) {
   }
 }
 
-void flce_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = std::max<uint64_t>(ns, 1000000ull); }
+void flce_set_wait_timeout_ns(uint64_t ns) {
+  g_timeout_ns.store(std::max<uint64_t>(ns, 1000000ull));
+  g_timeout_fixed.store(true);
+}
 
 const char* flce_kernel_name(int32_t kind) {
   switch (kind) {
@@ -676,6 +704,8 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
   flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
   if (st != FLCE_OK) return st;
   if (!loss || (T > 0 && (!lse || !logp))) return fail(FLCE_ERR_INVALID_ARG, "loss, lse or logp is NULL");
+  if (misaligned(loss) || misaligned(lse) || misaligned(logp) || misaligned(n_valid))
+    return fail(FLCE_ERR_ALIGNMENT, "loss, lse, logp (4 bytes) or n_valid (8 bytes) misaligned");
   if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
   if (workspace_bytes < flce_forward_workspace_size(T, Hd, V))
     return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
@@ -712,6 +742,8 @@ flce_status flce_score(const void* H, const void* W, const int64_t* targets, int
   flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, FLCE_REDUCTION_NONE);
   if (st != FLCE_OK) return st;
   if (T > 0 && !logp) return fail(FLCE_ERR_INVALID_ARG, "logp is NULL");
+  if (misaligned(logp) || misaligned(lse) || misaligned(argmax))
+    return fail(FLCE_ERR_ALIGNMENT, "logp, lse (4 bytes) or argmax (8 bytes) misaligned");
   if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
   if (workspace_bytes < flce_score_workspace_size(T, Hd, V))
     return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
@@ -755,6 +787,8 @@ flce_status flce_forward_shard(const void* H, const void* W_shard, const int64_t
   if (st != FLCE_OK) return st;
   if ((st = check_common(H, W_shard, targets, T, Hd, V_shard, -1, FLCE_REDUCTION_SUM)) != FLCE_OK) return st;
   if (T > 0 && (!shard_lse || !shard_zy)) return fail(FLCE_ERR_INVALID_ARG, "shard_lse or shard_zy is NULL");
+  if (misaligned(shard_lse) || misaligned(shard_zy))
+    return fail(FLCE_ERR_ALIGNMENT, "shard_lse and shard_zy must be 4-byte aligned");
   if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
   if (workspace_bytes < flce_forward_workspace_size(T, Hd, V_shard))
     return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
@@ -795,6 +829,9 @@ flce_status flce_combine_shards(const float* shard_lse, const float* shard_zy, i
     return fail(FLCE_ERR_INVALID_ARG, "ignore_index %lld lies inside [0, V_total)", (long long)ignore_index);
   if (!loss || (T > 0 && (!shard_lse || !shard_zy || !targets || !lse || !logp)))
     return fail(FLCE_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (misaligned(shard_lse) || misaligned(shard_zy) || misaligned(loss) || misaligned(lse) || misaligned(logp) ||
+      misaligned(n_valid) || misaligned(targets))
+    return fail(FLCE_ERR_ALIGNMENT, "a float array is not 4-byte or an int64 array not 8-byte aligned");
   if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
   if (workspace_bytes < flce_combine_workspace_size(T, n_shards))
     return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
@@ -831,6 +868,7 @@ flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* ta
     return fail(FLCE_ERR_WORKSPACE,
                 "T = %lld needs %zu bytes of scratch; the built-in scratch holds %zu bytes (T <= 253952)",
                 (long long)T, need, kStaticScratchBytes);
+  if (misaligned(device_status)) return fail(FLCE_ERR_ALIGNMENT, "device_status must be 4-byte aligned");
   void* scratch = nullptr;
   flce_status st = static_scratch_address(&scratch);
   if (st != FLCE_OK) return st;

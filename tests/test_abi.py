@@ -88,3 +88,34 @@ def test_argument_errors_return_before_any_launch(lib):
     st = lib.flce_forward(None, P(16), P(16), 10, 64, 50, -100, 1, P(16), P(16), P(16), None, P(256), 1 << 20, None)
     assert st == 1
     assert b"NULL" in lib.flce_last_error()
+
+
+def test_misaligned_typed_arrays_are_rejected_on_the_host(lib):
+    """Per-token arrays are accessed with typed loads and stores: a pointer off its
+    element alignment is an argument error, returned before anything is launched."""
+    P = ctypes.c_void_p
+    ok = dict(H=P(16), W=P(16), y=P(16), loss=P(16), lse=P(16), logp=P(16), nv=P(16))
+
+    def fwd(**kw):
+        a = {**ok, **kw}
+        return lib.flce_forward(a["H"], a["W"], a["y"], 10, 64, 50, -100, 1, a["loss"], a["lse"], a["logp"], a["nv"],
+                                P(256), 1 << 20, None)
+
+    assert fwd(y=P(20)) == 3       # targets (int64) off by 4
+    assert fwd(lse=P(18)) == 3     # float off by 2
+    assert fwd(logp=P(17)) == 3
+    assert fwd(loss=P(19)) == 3
+    assert fwd(nv=P(20)) == 3      # n_valid (int64) off by 4
+    st = lib.flce_backward(P(18), P(16), P(16), P(16), P(16), 10, 64, 50, -100, 1, P(16), P(16), P(256), 1 << 30,
+                           None)
+    assert st == 3                 # dloss off by 2
+    st = lib.flce_backward(P(16), P(16), P(16), P(16), P(22), 10, 64, 50, -100, 1, P(16), P(16), P(256), 1 << 30,
+                           None)
+    assert st == 3                 # lse off by 2
+    st = lib.flce_score(P(16), P(16), P(16), 10, 64, 50, -100, P(16), P(16), P(12), P(256), 1 << 30, None)
+    assert st == 3                 # argmax (int64) off by 4
+    st = lib.flce_combine_shards(P(16), P(18), 2, P(16), 10, 50, -100, 1, P(16), P(16), P(16), P(16), P(256), 1 << 20,
+                                 None)
+    assert st == 3                 # shard_zy off by 2
+    st = lib.flce_forward_shard(P(16), P(16), P(16), 10, 64, 25, 0, 50, -100, P(16), P(14), P(256), 1 << 20, None)
+    assert st == 3
