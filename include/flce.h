@@ -23,7 +23,10 @@
  *     *_workspace_size() function returns.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL means the legacy default stream).  Outputs are overwritten, never
- *     accumulated into.
+ *     accumulated into.  Outputs must not overlap one another, the inputs or
+ *     the workspace (not checked; overlapping buffers give undefined values).
+ *     One workspace serves one call at a time: calls that share a workspace
+ *     must be ordered on one stream.
  *   - Argument errors are detected on the host and returned before anything
  *     is launched.  Errors that depend on device data (a target outside
  *     [0, V) that is not ignore_index; a bounded wait inside a kernel that
