@@ -249,6 +249,39 @@ def test_full_size_workload(name, cuda_device):
     assert float(dW.abs().max().item()) > 0.0
 
 
+def test_dz_block_beyond_2_31_elements(cuda_device):
+    """A backward workspace holding one 8192-token chunk of a 300,001-row vocabulary:
+    the dZ block has 8192 x 300,032 = 2.46e9 elements (4.9 GB), past 32-bit element
+    offsets.  Sampled token rows against the oracle; dW through the invariants."""
+    T, Hd, V = 8192, 64, 300001
+    inp = generate("medium", T=T, Hd=Hd, V=V)
+    v_pad = (V + 63) // 64 * 64
+    ws = flce.flce_backward_workspace_size(T, Hd, V)
+    ws += 2 * (8192 - flce.flce_backward_chunk_tokens(T, Hd, V, ws)) * v_pad
+    assert flce.flce_backward_chunk_tokens(T, Hd, V, ws) == 8192 and 8192 * v_pad > 2 ** 31
+    out = run(inp, cuda_device, bwd_workspace_bytes=ws)
+    assert out["fwd_status"] == 0 and out["bwd_status"] == 0
+    valid = inp.targets != inp.ignore_index
+    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(9).choice(T, 30, replace=False)]))
+    W64 = inp.W64()
+    g = oracle.upstream_grad(inp.dloss, inp.targets, V, inp.ignore_index, inp.reduction)
+    ref = oracle.sampled_rows(inp.H64(rows), W64, inp.targets[rows], g[rows], inp.ignore_index)
+    check_token_outputs(out, ref, valid[rows], inp.reduction, rows=rows)
+    dH = out["dH"].float()
+    dH_rows = dH[torch.from_numpy(rows).to(cuda_device)].cpu().numpy()
+    assert rel_fro(dH_rows, ref["dH"]) <= TOL_GRAD
+    H_dev, W_dev = to_device(inp, cuda_device)[:2]
+    dW = out["dW"]
+    colsum = dW.double().sum(dim=0).cpu().numpy()
+    hnorm = H_dev.float().norm(dim=1).double().cpu().numpy()
+    assert np.linalg.norm(colsum) <= 2.0 ** -8 * float(np.sum(np.abs(g) * hnorm)) + 1e-6
+    lhs = float((dW.double() * W_dev.double()).sum().item())
+    rhs = float((dH.double() * H_dev.double()).sum().item())
+    assert abs(lhs - rhs) <= TOL_GRAD * max(abs(lhs), abs(rhs)) + 1e-6
+    # the last vocab rows (beyond 2^31 / 8192 columns into the block) carry gradient too
+    assert float(dW[-64:].abs().max().item()) > 0.0
+
+
 def test_full_size_sampled_dW_medium(cuda_device):
     """Sampled vocab rows of dW at the full medium size (T=8192, Hd=2048, V=124,160) against
     the oracle; needs the oracle's lse on every token (one fp64 pass over T x V)."""
