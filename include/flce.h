@@ -87,13 +87,22 @@ typedef enum flce_reduction {
 FLCE_API size_t flce_forward_workspace_size(int64_t T, int64_t Hd, int64_t V);
 
 /* Bytes of workspace flce_backward() needs to run with its default token
- * chunk.  The backward works on token chunks of `chunk` rows; the workspace
- * holds one [chunk x V] bf16 slice of dZ (the page's [block x vocab]
- * residency) plus O(T) scalars.  The default chunk is below T whenever
- * T > 256, so the workspace stays below the T*V*2 bytes of one dense bf16
- * logits tensor.  A larger or smaller workspace is accepted: the backward then
- * uses the largest chunk (a multiple of 128 tokens, at least 128) that fits. */
+ * chunk.  The backward skips the rows whose upstream gradient g_t is zero
+ * (ignored targets; their dZ rows vanish) and works on chunks of `chunk` of
+ * the remaining rows, in token order; the workspace holds one [chunk x V] bf16
+ * slice of dZ (the page's [block x vocab] residency), the chunk's rows of H
+ * and dH ([chunk x Hd] bf16 each) and O(T) scalars.  The default chunk is
+ * min(8192, T/2 rounded down to 128) (128 below T = 256), so for T > 256 and
+ * Hd < V/2 the workspace stays below the T*V*2 bytes of one dense bf16 logits
+ * tensor.  A larger or smaller workspace is accepted:
+ * the backward then uses the largest chunk (a multiple of 128 rows, at least
+ * 128) that fits. */
 FLCE_API size_t flce_backward_workspace_size(int64_t T, int64_t Hd, int64_t V);
+
+/* Bytes of backward workspace for chunks of `chunk` rows (a positive multiple
+ * of 128; chunks above T rounded up to 128 are capped there); 0 for an invalid
+ * chunk or size. */
+FLCE_API size_t flce_backward_workspace_size_for_chunk(int64_t T, int64_t Hd, int64_t V, int64_t chunk);
 
 /* The token chunk flce_backward() uses with a workspace of `workspace_bytes`;
  * 0 if the workspace is too small. */
@@ -266,7 +275,10 @@ FLCE_API void flce_set_wait_timeout_ns(uint64_t ns);
  * events recorded on its launch stream.  flce_profile_collect() synchronizes
  * on those events and returns, per kernel kind, the launches, the summed
  * device time and the summed algorithmic work (FLOPs and bytes the kernel's
- * mathematics requires, independent of how it is executed). */
+ * mathematics requires, independent of how it is executed).  The backward's
+ * work is counted over the rows it does not skip; that count is read from the
+ * backward workspace at collection time, so collect while the workspaces of
+ * the profiled calls still exist (each reports its latest call). */
 typedef struct flce_kernel_stats {
   int32_t kind;     /* flce_kernel_kind value */
   int32_t launches;
@@ -282,7 +294,9 @@ typedef enum flce_kernel_kind {
   FLCE_KERNEL_BWD_PREP = 3,       /* n_valid and the per-token upstream weights g */
   FLCE_KERNEL_BWD_DZ = 4,         /* recomputed logit tiles + dZ epilogue, bf16 dZ chunk */
   FLCE_KERNEL_BWD_DH_DW = 5,      /* dH chunk = dZ W and dW (+)= dZ^T H, one launch per chunk */
-  FLCE_KERNEL_KINDS = 6
+  FLCE_KERNEL_BWD_GATHER = 6,     /* the chunk's rows of H gathered through the row list */
+  FLCE_KERNEL_BWD_SCATTER = 7,    /* the chunk's dH rows written back to their tokens */
+  FLCE_KERNEL_KINDS = 8
 } flce_kernel_kind;
 
 FLCE_API void flce_profile_enable(int32_t on);

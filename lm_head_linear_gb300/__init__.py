@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     SIGNATURES,
     flce_backward,
     flce_backward_chunk_tokens,
+    flce_backward_workspace_size_for_chunk,
     flce_backward_shard,
     flce_combine_shards,
     flce_backward_workspace_size,

@@ -22,7 +22,7 @@ STATUS_NAMES = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_ALIGNMENT",
     4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
 }
-KERNEL_KINDS = 6
+KERNEL_KINDS = 8
 
 # Every symbol the header declares: name -> (restype, argtypes).
 _P = ctypes.c_void_p
@@ -31,6 +31,7 @@ _I32 = ctypes.c_int32
 SIGNATURES = {
     "flce_forward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "flce_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "flce_backward_workspace_size_for_chunk": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "flce_backward_chunk_tokens": (_I64, [_I64, _I64, _I64, ctypes.c_size_t]),
     "flce_forward": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P]),
@@ -140,6 +141,10 @@ def flce_forward_workspace_size(T: int, Hd: int, V: int) -> int:
 
 def flce_backward_workspace_size(T: int, Hd: int, V: int) -> int:
     return int(load_library().flce_backward_workspace_size(T, Hd, V))
+
+
+def flce_backward_workspace_size_for_chunk(T: int, Hd: int, V: int, chunk: int) -> int:
+    return int(load_library().flce_backward_workspace_size_for_chunk(T, Hd, V, chunk))
 
 
 def flce_backward_chunk_tokens(T: int, Hd: int, V: int, workspace_bytes: int) -> int:

@@ -166,6 +166,11 @@ struct LaunchRecord {
   int kind;
   cudaEvent_t start, stop;
   double flops, bytes;
+  // Launches over the backward's row list add rows * (flops, bytes) per row, the
+  // rows read from the workspace when the records are collected.
+  const int32_t* rows_dev;
+  int64_t index0, cap;
+  double flops_per_row, bytes_per_row;
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -190,7 +195,9 @@ struct KernelScope {
   bool nvtx = true;
   LaunchRecord rec{};
   cudaStream_t stream;
-  KernelScope(int kind, cudaStream_t s, double flops, double bytes) : stream(s) {
+  KernelScope(int kind, cudaStream_t s, double flops, double bytes, const int32_t* rows_dev = nullptr,
+              int64_t index0 = 0, int64_t cap = 0, double flops_per_row = 0.0, double bytes_per_row = 0.0)
+      : stream(s) {
     nvtxRangePushA(flce_kernel_name(kind));
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on) return;
@@ -198,6 +205,11 @@ struct KernelScope {
     rec.kind = kind;
     rec.flops = flops;
     rec.bytes = bytes;
+    rec.rows_dev = rows_dev;
+    rec.index0 = index0;
+    rec.cap = cap;
+    rec.flops_per_row = flops_per_row;
+    rec.bytes_per_row = bytes_per_row;
     rec.start = take_event();
     rec.stop = take_event();
     cudaEventRecord(rec.start, s);
@@ -254,20 +266,31 @@ struct BwdLayout {
   int64_t chunk;
   int64_t v_pad;
   int64_t max_chunks;
-  size_t cnt_off, g_off, dz_off, total;
+  size_t cnt_off, g_off, idx_off, hc_off, dhc_off, dz_off, total;
 };
 
-// Header | tile counters (one per possible chunk) | g [T] | dZ chunk [chunk, V_pad].
-BwdLayout bwd_layout(int64_t T, int64_t V, int64_t chunk) {
+constexpr size_t kRowCountOff = 16;  // backward header: length of the row list (int32)
+
+// Header (status word, row count) | tile counters (one per possible chunk) |
+// g [T] | row list [T] | H rows of the chunk [chunk, Hd] | dH rows of the chunk
+// [chunk, Hd] | dZ chunk [chunk, V_pad].
+BwdLayout bwd_layout(int64_t T, int64_t Hd, int64_t V, int64_t chunk) {
   BwdLayout L{};
   L.chunk = chunk;
   L.v_pad = static_cast<int64_t>(align_up(static_cast<size_t>(V), 64));
   L.max_chunks = cdiv(std::max<int64_t>(T, 1), 128);
+  const size_t t1 = static_cast<size_t>(std::max<int64_t>(T, 1));
   size_t off = kHeaderBytes;
   L.cnt_off = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L.max_chunks), 256);
   L.g_off = off;
-  off = align_up(off + sizeof(float) * static_cast<size_t>(std::max<int64_t>(T, 1)), 1024);
+  off = align_up(off + sizeof(float) * t1, 256);
+  L.idx_off = off;
+  off = align_up(off + sizeof(int32_t) * t1, 1024);
+  L.hc_off = off;
+  off = align_up(off + 2ull * static_cast<size_t>(chunk) * static_cast<size_t>(Hd), 1024);
+  L.dhc_off = off;
+  off = align_up(off + 2ull * static_cast<size_t>(chunk) * static_cast<size_t>(Hd), 1024);
   L.dz_off = off;
   off = align_up(off + 2ull * static_cast<size_t>(chunk) * L.v_pad, 256);
   L.total = off;
@@ -275,8 +298,9 @@ BwdLayout bwd_layout(int64_t T, int64_t V, int64_t chunk) {
 }
 
 int64_t default_chunk(int64_t T) {
-  // Below T whenever T > 256, so dZ residency stays [chunk x V] < [T x V].
-  int64_t c = static_cast<int64_t>(align_up(static_cast<size_t>(cdiv(std::max<int64_t>(T, 1), 2)), 128));
+  // At most T / 2 whenever T >= 256, so dZ residency stays [chunk x V] <= [T/2 x V],
+  // and the whole workspace below one [T x V] bf16 tensor whenever Hd < V / 2.
+  int64_t c = std::max<int64_t>(T, 0) / 2 / 128 * 128;
   c = std::max<int64_t>(c, 128);
   return std::min<int64_t>(c, kDefaultChunk);
 }
@@ -476,46 +500,66 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     CUDA_TRY(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * Hd, s));
     return FLCE_OK;
   }
-  const BwdLayout L = bwd_layout(T, V, chunk);
+  const BwdLayout L = bwd_layout(T, Hd, V, chunk);
   float* g = reinterpret_cast<float*>(ws + L.g_off);
+  int32_t* row_index = reinterpret_cast<int32_t*>(ws + L.idx_off);
+  int32_t* row_count = reinterpret_cast<int32_t*>(ws + kRowCountOff);
+  void* Hc = ws + L.hc_off;
+  void* dHc = ws + L.dhc_off;
   void* dz = ws + L.dz_off;
 
+  // Rows whose g_t is zero have zero dZ rows: their dH rows are zero and they add
+  // nothing to dW, so the contractions run over the list of the other rows only.
+  CUDA_TRY(cudaMemsetAsync(dH, 0, 2 * static_cast<size_t>(T) * Hd, s));
   {
-    KernelScope ks(FLCE_KERNEL_BWD_PREP, s, 0.0, 12.0 * T);
+    KernelScope ks(FLCE_KERNEL_BWD_PREP, s, 0.0, 20.0 * T);
     bwd_prep_kernel<<<1, kReduceThreads, 0, s>>>(dloss, dlogp, targets, static_cast<int>(T),
-                                                 static_cast<int>(V_total), ignore_index, reduction, g, status);
+                                                 static_cast<int>(V_total), ignore_index, reduction, g, row_index,
+                                                 row_count, status);
     ks.done();
     if ((st = check_launch("bwd_prep")) != FLCE_OK) return st;
   }
   const int64_t n_hd_blocks = cdiv(Hd, BN);
-  CUtensorMap tm_H_k, tm_W_k, tm_W_mn, tm_H_mn, tm_dH, tm_dW_out;
-  if ((st = make_map(&tm_H_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, BK, BM)) != FLCE_OK) return st;
+  CUtensorMap tm_Hc_k, tm_W_k, tm_W_mn, tm_Hc_mn, tm_dHc, tm_dW_out, tm_dz_store, tm_dz_k, tm_dz_mn;
+  if ((st = make_map(&tm_Hc_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hc, Hd, chunk, Hd * 2, BK, BM)) != FLCE_OK) return st;
   if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
   if ((st = make_map(&tm_W_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, 64, 64)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_H_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Hd, T, Hd * 2, 64, 64)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_dH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dH, Hd, T, Hd * 2, 64, 32)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_Hc_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hc, Hd, chunk, Hd * 2, 64, 64)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_dHc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dHc, Hd, chunk, Hd * 2, 64, 32)) != FLCE_OK) return st;
   if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
+  if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, chunk, L.v_pad * 2, 64, 32)) != FLCE_OK)
+    return st;
+  if ((st = make_map(&tm_dz_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, chunk, L.v_pad * 2, BK, BM)) != FLCE_OK)
+    return st;
+  if ((st = make_map(&tm_dz_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, chunk, L.v_pad * 2, 64, 64)) != FLCE_OK)
+    return st;
 
   const int64_t n_chunks = cdiv(T, chunk);
   int32_t* counters = reinterpret_cast<int32_t*>(ws + L.cnt_off);
   CUDA_TRY(cudaMemsetAsync(counters, 0, sizeof(int32_t) * static_cast<size_t>(n_chunks), s));
+  const int row_vecs = static_cast<int>(Hd / 8);  // 16-byte pieces of a bf16 row
+  const int copy_grid =
+      static_cast<int>(std::min<int64_t>(cdiv(chunk * row_vecs, kCopyThreads), 8 * static_cast<int64_t>(dev->sms)));
+  const int64_t cap_pairs = cdiv(chunk, 2 * BM);
 
   for (int64_t c = 0; c < n_chunks; ++c) {
-    const int64_t c0 = c * chunk;
-    const int64_t rows = std::min<int64_t>(chunk, T - c0);
-    const int64_t m_pairs = cdiv(rows, 2 * BM);
-    CUtensorMap tm_dz_store, tm_dz_k, tm_dz_mn;
-    if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 32)) != FLCE_OK)
-      return st;
-    if ((st = make_map(&tm_dz_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, BK, BM)) != FLCE_OK)
-      return st;
-    if ((st = make_map(&tm_dz_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, rows, L.v_pad * 2, 64, 64)) != FLCE_OK)
-      return st;
+    const int64_t c0 = c * chunk;  // list position of the chunk's first row
+    {
+      KernelScope ks(FLCE_KERNEL_BWD_GATHER, s, 0.0, 0.0, row_count, c0, chunk, 0.0, 4.0 * Hd + 4.0);
+      gather_rows_kernel<<<copy_grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(H), row_index, row_count,
+                                                            static_cast<int>(c0), static_cast<int>(chunk), row_vecs,
+                                                            static_cast<uint4*>(Hc));
+      ks.done();
+      if ((st = check_launch("bwd_gather")) != FLCE_OK) return st;
+    }
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    p.row0 = static_cast<int32_t>(c0);
-    p.rows = static_cast<int32_t>(rows);
+    p.row0 = 0;
+    p.rows = static_cast<int32_t>(chunk);  // capacity; the kernels take the chunk's share of the list
+    p.rows_dev = row_count;
+    p.row_index = row_index;
+    p.index0 = static_cast<int32_t>(c0);
     p.T = static_cast<int32_t>(T);
     p.V = static_cast<int32_t>(V);
     p.vocab_offset = vocab_offset;
@@ -528,17 +572,17 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     p.n_split = 1;
 
     // (1) recomputed logit tiles -> dZ chunk
-    p.tmA = tm_H_k;
+    p.tmA = tm_Hc_k;
     p.tmB = tm_W_k;
     p.tmOut = tm_dz_store;
-    p.num_m_pairs = static_cast<int32_t>(m_pairs);
+    p.num_m_pairs = static_cast<int32_t>(cap_pairs);
     p.num_n_blocks = static_cast<int32_t>(cdiv(V, BN));
     p.num_k_blocks = static_cast<int32_t>(Hd / BK);
     p.num_units = p.num_m_pairs * p.num_n_blocks;
     {
       const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DZ], p.num_units));
-      KernelScope ks(FLCE_KERNEL_BWD_DZ, s, 2.0 * rows * Hd * V,
-                     2.0 * (rows * Hd + V * Hd) + 2.0 * rows * V + 16.0 * rows);
+      KernelScope ks(FLCE_KERNEL_BWD_DZ, s, 0.0, 2.0 * V * Hd, row_count, c0, chunk, 2.0 * Hd * V,
+                     2.0 * Hd + 2.0 * V + 16.0);
       gemm_kernel<MODE_DZ><<<grid, kThreads, smem_bytes_for(MODE_DZ), s>>>(p);
       ks.done();
       if ((st = check_launch("bwd_dz")) != FLCE_OK) return st;
@@ -547,25 +591,35 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     //     the first chunk stores dW, later chunks add to it, in chunk order.
     p.tmA = tm_dz_k;
     p.tmB = tm_W_mn;
-    p.tmOut = tm_dH;
+    p.tmOut = tm_dHc;
     p.tmA2 = tm_dz_mn;
-    p.tmB2 = tm_H_mn;
+    p.tmB2 = tm_Hc_mn;
     p.tmOut2 = tm_dW_out;
     p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
     p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
-    p.num_k_blocks2 = static_cast<int32_t>(cdiv(rows, BK));
-    p.n_dh_tiles = static_cast<int32_t>(m_pairs * n_hd_blocks);
+    p.num_k_blocks2 = static_cast<int32_t>(cdiv(chunk, BK));
+    p.n_dh_tiles = static_cast<int32_t>(cap_pairs * n_hd_blocks);
     p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
     p.reduce_out = c > 0 ? 1 : 0;
     p.tile_counter = counters + c;
-    p.timeout_ns = wait_limit_ns(std::max<int64_t>(V, rows));  // dH tiles: K = V; dW tiles: K = rows
+    p.dW_zero = dW;
+    p.dW_elems = V * Hd;
+    p.timeout_ns = wait_limit_ns(std::max<int64_t>(V, chunk));  // dH tiles: K = V; dW tiles: K = the chunk
     {
       const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DHW], p.n_dh_tiles + p.n_dw_tiles));
-      KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 4.0 * rows * Hd * V,
-                     4.0 * rows * V + 2.0 * V * Hd + 4.0 * rows * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd);
+      KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 0.0, 2.0 * V * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd, row_count, c0,
+                     chunk, 4.0 * Hd * V, 4.0 * V + 4.0 * Hd);
       gemm_kernel<MODE_DHW><<<grid, kThreads, smem_bytes_for(MODE_DHW), s>>>(p);
       ks.done();
       if ((st = check_launch("bwd_dh_dw")) != FLCE_OK) return st;
+    }
+    {
+      KernelScope ks(FLCE_KERNEL_BWD_SCATTER, s, 0.0, 0.0, row_count, c0, chunk, 0.0, 4.0 * Hd + 4.0);
+      scatter_rows_kernel<<<copy_grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(dHc), row_index, row_count,
+                                                             static_cast<int>(c0), static_cast<int>(chunk), row_vecs,
+                                                             static_cast<uint4*>(dH));
+      ks.done();
+      if ((st = check_launch("bwd_scatter")) != FLCE_OK) return st;
     }
   }
   return FLCE_OK;
@@ -607,6 +661,8 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_KERNEL_BWD_PREP: return "bwd_prep";
     case FLCE_KERNEL_BWD_DZ: return "bwd_dz";
     case FLCE_KERNEL_BWD_DH_DW: return "bwd_dh_dw";
+    case FLCE_KERNEL_BWD_GATHER: return "bwd_gather";
+    case FLCE_KERNEL_BWD_SCATTER: return "bwd_scatter";
     default: return "unknown";
   }
 }
@@ -629,10 +685,19 @@ flce_status flce_profile_collect(flce_kernel_stats* out, int32_t max_entries, in
     float ms = 0.0f;
     if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
       st = fail(FLCE_ERR_CUDA, "event query failed");
+    double flops = r.flops, bytes = r.bytes;
+    if (r.rows_dev) {
+      int32_t n = 0;
+      if (cudaMemcpy(&n, r.rows_dev, sizeof(n), cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(FLCE_ERR_CUDA, "reading a row count failed");
+      const double rows = static_cast<double>(std::min<int64_t>(std::max<int64_t>(n - r.index0, 0), r.cap));
+      flops += rows * r.flops_per_row;
+      bytes += rows * r.bytes_per_row;
+    }
     agg[r.kind].launches += 1;
     agg[r.kind].total_ms += ms;
-    agg[r.kind].flops += r.flops;
-    agg[r.kind].bytes += r.bytes;
+    agg[r.kind].flops += flops;
+    agg[r.kind].bytes += bytes;
   }
   {
     std::lock_guard<std::mutex> lk(g_prof_mu);
@@ -655,21 +720,27 @@ size_t flce_forward_workspace_size(int64_t T, int64_t Hd, int64_t V) {
 }
 
 size_t flce_backward_workspace_size(int64_t T, int64_t Hd, int64_t V) {
-  (void)Hd;
-  if (T < 0 || V < 1) return 0;
-  return bwd_layout(T, V, default_chunk(T)).total;
+  if (T < 0 || V < 1 || Hd < 1) return 0;
+  return bwd_layout(T, Hd, V, default_chunk(T)).total;
+}
+
+size_t flce_backward_workspace_size_for_chunk(int64_t T, int64_t Hd, int64_t V, int64_t chunk) {
+  if (T < 0 || V < 1 || Hd < 1 || chunk < 128 || chunk % 128 != 0) return 0;
+  const int64_t cap = static_cast<int64_t>(align_up(static_cast<size_t>(std::max<int64_t>(T, 1)), 128));
+  return bwd_layout(T, Hd, V, std::min(chunk, cap)).total;
 }
 
 int64_t flce_backward_chunk_tokens(int64_t T, int64_t Hd, int64_t V, size_t workspace_bytes) {
-  (void)Hd;
-  if (T < 0 || V < 1) return 0;
+  if (T < 0 || V < 1 || Hd < 1) return 0;
   const int64_t cap = static_cast<int64_t>(align_up(static_cast<size_t>(std::max<int64_t>(T, 1)), 128));
-  const BwdLayout L0 = bwd_layout(T, V, 0);
+  const BwdLayout L0 = bwd_layout(T, Hd, V, 0);
   if (workspace_bytes < L0.total) return 0;
-  const size_t per_row = 2ull * static_cast<size_t>(L0.v_pad);
-  int64_t c = static_cast<int64_t>((workspace_bytes - L0.dz_off) / per_row);
-  c = c / 128 * 128;
-  c = std::min(c, cap);
+  // per chunk row: its dZ row, its H row and its dH row; the regions' alignment
+  // padding (a few KB) can cost one step of 128 rows
+  const size_t per_row = 2ull * static_cast<size_t>(L0.v_pad) + 4ull * static_cast<size_t>(Hd);
+  int64_t c = static_cast<int64_t>((workspace_bytes - L0.hc_off) / per_row);
+  c = std::min(c / 128 * 128, cap);
+  while (c >= 128 && bwd_layout(T, Hd, V, c).total > workspace_bytes) c -= 128;
   return c < 128 ? 0 : c;
 }
 

@@ -124,7 +124,45 @@ struct GemmParams {
   int32_t* tile_counter; // MODE_DHW: zero before the launch
   int32_t* status;
   uint64_t timeout_ns;
+  // MODE_DZ / MODE_DHW over compacted rows (the backward skips rows whose upstream
+  // gradient is zero): the chunk holds list positions index0 .. index0 + rows - 1 of
+  // the row list, whose length the prep kernel writes to *rows_dev; token rows of
+  // H / dH come gathered in the chunk's own buffers, and targets, lse and g are
+  // read through row_index.  rows_dev == nullptr: rows row0 .. row0 + rows - 1.
+  const int32_t* rows_dev;
+  const int32_t* row_index;
+  int32_t index0;
+  float* dW_zero;        // MODE_DHW: dW, zero-filled here when the list is empty
+  int64_t dW_elems;
 };
+
+// Extent of one launch: the host's figures, or, over compacted rows, the ones
+// that follow from the chunk's share of the row list.
+struct Counts {
+  int rows;           // rows of the chunk
+  int num_m_pairs;    // 256-row pairs along M (static modes) / dH tiles' token pairs
+  int num_units;      // static modes: work units
+  int n_dh_tiles;     // MODE_DHW
+  int num_k_blocks2;  // MODE_DHW: K blocks of a dW tile
+};
+
+__device__ __forceinline__ Counts counts_of(const GemmParams& p) {
+  Counts c;
+  if (!p.rows_dev) {
+    c.rows = p.rows;
+    c.num_m_pairs = p.num_m_pairs;
+    c.num_units = p.num_units;
+    c.n_dh_tiles = p.n_dh_tiles;
+    c.num_k_blocks2 = p.num_k_blocks2;
+    return c;
+  }
+  c.rows = min(max(*p.rows_dev - p.index0, 0), p.rows);
+  c.num_m_pairs = (c.rows + 2 * BM - 1) / (2 * BM);
+  c.num_units = c.num_m_pairs * p.num_n_blocks;
+  c.n_dh_tiles = c.num_m_pairs * p.num_n_blocks;
+  c.num_k_blocks2 = (c.rows + BK - 1) / BK;
+  return c;
+}
 
 struct Unit {
   int m_blk;
@@ -135,7 +173,7 @@ struct Unit {
 
 // Work unit of a pair; m_blk is this CTA's 128-row block (2 * pair + rank).
 template <int MODE>
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, uint32_t rank) {
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const Counts& c, int u, uint32_t rank) {
   Unit r;
   if constexpr (is_forward(MODE)) {
     // Vocab ranges are taken two at a time (when n_split is even): units
@@ -144,7 +182,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, uint32_t
     // hold half as many H blocks, which keeps both in L2 (forward DRAM reads
     // 25 GB -> 10 GB at 65,536 x 2048 x 124,160).
     const int G = (p.n_split % 2 == 0) ? 2 : 1;
-    const int gsz = G * p.num_m_pairs;
+    const int gsz = G * c.num_m_pairs;
     const int grp = u / gsz;
     const int rr = u - grp * gsz;
     const int split = grp * G + rr % G;
@@ -155,8 +193,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, uint32_t
     r.n_lo = split * base + min(split, rem);
     r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
   } else {
-    const int nb = u / p.num_m_pairs;  // token blocks fastest: the W tile is shared in L2
-    r.m_blk = 2 * (u - nb * p.num_m_pairs) + static_cast<int>(rank);
+    const int nb = u / c.num_m_pairs;  // token blocks fastest: the W tile is shared in L2
+    r.m_blk = 2 * (u - nb * c.num_m_pairs) + static_cast<int>(rank);
     r.n_lo = nb;
     r.n_hi = nb + 1;
     r.split = 0;
@@ -173,14 +211,14 @@ struct Tile {
   int num_k;
 };
 
-__device__ __forceinline__ Tile decode_dhw(const GemmParams& p, int t, uint32_t rank) {
+__device__ __forceinline__ Tile decode_dhw(const GemmParams& p, const Counts& c, int t, uint32_t rank) {
   Tile r;
-  r.family = t < p.n_dh_tiles ? 0 : 1;
-  const int u = r.family ? t - p.n_dh_tiles : t;
+  r.family = t < c.n_dh_tiles ? 0 : 1;
+  const int u = r.family ? t - c.n_dh_tiles : t;
   const int pair = u / p.num_n_blocks;
   r.nb = u - pair * p.num_n_blocks;
   r.m_blk = 2 * pair + static_cast<int>(rank);
-  r.num_k = r.family ? p.num_k_blocks2 : p.num_k_blocks;
+  r.num_k = r.family ? c.num_k_blocks2 : p.num_k_blocks;
   return r;
 }
 
@@ -435,11 +473,12 @@ __device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce,
 // ----------------------------------------------------------------------------- MODE_FWD / MODE_DZ loops (static schedule)
 // Pair c of the grid takes units c, c + pairs, c + 2 * pairs, ...
 template <int MODE>
-__device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLayout& s, uint32_t rank) {
+__device__ __forceinline__ void producer_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
+                                              uint32_t rank) {
   ProducerState ps;
   bool ok = true;
-  for (int u = blockIdx.x >> 1; u < p.num_units && ok; u += gridDim.x >> 1) {
-    const Unit un = decode_unit<MODE>(p, u, rank);
+  for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
+    const Unit un = decode_unit<MODE>(p, c, u, rank);
     for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb)
       ok = produce_tile(p, s, ps, 0, un.m_blk, nb, p.num_k_blocks, rank);
   }
@@ -448,12 +487,13 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, const SmemLay
 
 // Even CTA only.
 template <int MODE>
-__device__ __forceinline__ void mma_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
+__device__ __forceinline__ void mma_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
+                                         uint32_t tmem_base) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN, 0, 0);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int u = blockIdx.x >> 1; u < p.num_units && ok; u += gridDim.x >> 1) {
-    const Unit un = decode_unit<MODE>(p, u, 0);
+  for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
+    const Unit un = decode_unit<MODE>(p, c, u, 0);
     for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
       if (!ptx::wait_bounded_cluster(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
         abort_cta(p, s);
@@ -481,8 +521,8 @@ __device__ __forceinline__ void release_accumulator(const SmemLayout& s, uint32_
 }
 
 template <int MODE>
-__device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base,
-                                              int warp, int lane, uint32_t rank) {
+__device__ __forceinline__ void epilogue_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
+                                              uint32_t tmem_base, int warp, int lane, uint32_t rank) {
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const int row_in_tile = q * 32 + lane;
   const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -491,9 +531,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
   bool ok = true;
 
-  for (int u = blockIdx.x >> 1; u < p.num_units && ok; u += gridDim.x >> 1) {
-    const Unit un = decode_unit<MODE>(p, u, rank);
-    const bool active = un.m_blk * BM < p.rows;       // the odd CTA of a ragged last pair has no rows
+  for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
+    const Unit un = decode_unit<MODE>(p, c, u, rank);
+    const bool active = un.m_blk * BM < c.rows;       // the odd CTA of a ragged last pair has no rows
     const int t_local = un.m_blk * BM + row_in_tile;  // token within the launch
 
     float m_run = -INFINITY, s_run = 0.0f, zy = 0.0f;
@@ -504,13 +544,13 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
     int best_col = -1;
     // y: the target's local vocab column when this launch's vocab rows own it, else -1
     if constexpr (is_forward(MODE)) {
-      if (t_local < p.rows) {
+      if (t_local < c.rows) {
         const int64_t yy = p.targets[t_local] - p.vocab_offset;
         if (p.targets[t_local] != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
       }
     } else {
-      if (t_local < p.rows) {
-        const int t = p.row0 + t_local;
+      if (t_local < c.rows) {
+        const int t = p.row_index ? p.row_index[p.index0 + t_local] : p.row0 + t_local;
         gt = p.g[t];
         lse2 = p.lse[t] * kLog2e;
         const int64_t yy = p.targets[t] - p.vocab_offset;
@@ -579,7 +619,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const SmemLay
     }
 
     if constexpr (is_forward(MODE)) {
-      if (ok && t_local < p.rows) {
+      if (ok && t_local < c.rows) {
         p.partials[static_cast<size_t>(un.split) * p.part_stride + t_local] = make_float2(m_run, s_run);
         if (have_zy) p.zy[t_local] = zy;
         if constexpr (MODE == MODE_SCORE) {
@@ -605,9 +645,10 @@ __device__ __forceinline__ uint32_t ring_addr(const SmemLayout& s, int slot) {
   return ptx::smem_u32(const_cast<int*>(s.tile_ring + slot));
 }
 
-__device__ __forceinline__ void dhw_producer(const GemmParams& p, const SmemLayout& s, uint32_t rank) {
+__device__ __forceinline__ void dhw_producer(const GemmParams& p, const Counts& c, const SmemLayout& s,
+                                             uint32_t rank) {
   ProducerState ps;
-  const int total = p.n_dh_tiles + p.n_dw_tiles;
+  const int total = c.n_dh_tiles + p.n_dw_tiles;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
     const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
@@ -631,17 +672,18 @@ __device__ __forceinline__ void dhw_producer(const GemmParams& p, const SmemLayo
       ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     }
     if (t >= total) break;
-    const Tile ti = decode_dhw(p, t, rank);
+    const Tile ti = decode_dhw(p, c, t, rank);
     if (!produce_tile(p, s, ps, 1 + ti.family, ti.m_blk, ti.nb, ti.num_k, rank)) break;
   }
   ps.drain(s, rank);
 }
 
 // Even CTA only.
-__device__ __forceinline__ void dhw_mma(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base) {
+__device__ __forceinline__ void dhw_mma(const GemmParams& p, const Counts& c, const SmemLayout& s,
+                                        uint32_t tmem_base) {
   constexpr uint32_t idesc_dh = ptx::idesc_bf16_f32(2 * BM, BN, 0, 1);
   constexpr uint32_t idesc_dw = ptx::idesc_bf16_f32(2 * BM, BN, 1, 1);
-  const int total = p.n_dh_tiles + p.n_dw_tiles;
+  const int total = c.n_dh_tiles + p.n_dw_tiles;
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
@@ -653,7 +695,7 @@ __device__ __forceinline__ void dhw_mma(const GemmParams& p, const SmemLayout& s
     const int t = s.tile_ring[slot];
     ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     if (t >= total) break;
-    const Tile ti = decode_dhw(p, t, 0);
+    const Tile ti = decode_dhw(p, c, t, 0);
     if (!ptx::wait_bounded_cluster(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       break;
@@ -670,12 +712,12 @@ __device__ __forceinline__ void dhw_mma(const GemmParams& p, const SmemLayout& s
   ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
 }
 
-__device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayout& s, uint32_t tmem_base, int warp,
-                                             int lane, uint32_t rank) {
+__device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const Counts& c, const SmemLayout& s,
+                                             uint32_t tmem_base, int warp, int lane, uint32_t rank) {
   const int q = warp & 3;
   const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
-  const int total = p.n_dh_tiles + p.n_dw_tiles;
+  const int total = c.n_dh_tiles + p.n_dw_tiles;
   uint32_t acc = 0, acc_phase = 0, box_count = 0;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
@@ -688,7 +730,7 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayo
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     if (t >= total) break;
-    const Tile ti = decode_dhw(p, t, rank);
+    const Tile ti = decode_dhw(p, c, t, rank);
     if (!ptx::wait_bounded_cluster(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       break;
@@ -696,7 +738,7 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const SmemLayo
     ptx::tc_fence_after();
     const uint32_t tcol = lane_addr + acc * BN;
     if (ti.family == 0) {
-      if (ti.m_blk * BM < p.rows)
+      if (ti.m_blk * BM < c.rows)
         epi_bf16_tile<false>(&p.tmOut, tcol, ti.nb * BN, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count,
                              lane, 0.0f, 0.0f, -1);
     } else {
@@ -717,6 +759,25 @@ template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
+  const Counts c = counts_of(p);
+  if (p.rows_dev && c.rows == 0) {
+    // An empty chunk of the row list: nothing to compute.  Every CTA sees the same
+    // count and leaves before any barrier, TMEM or cluster operation.  When the
+    // list is empty altogether, the first chunk's dW (stored, not added to) is zero.
+    if constexpr (MODE == MODE_DHW) {
+      if (!p.reduce_out && p.dW_zero) {
+        const int64_t n4 = p.dW_elems / 4;
+        float4* d4 = reinterpret_cast<float4*>(p.dW_zero);
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+          d4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int64_t i = n4 * 4 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.dW_elems;
+             i += stride)
+          p.dW_zero[i] = 0.0f;
+      }
+    }
+    return;
+  }
   const SmemLayout s = carve_smem<MODE>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -764,24 +825,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (ptx::elect_one()) {
       if constexpr (MODE == MODE_DHW)
-        dhw_producer(p, s, rank);
+        dhw_producer(p, c, s, rank);
       else
-        producer_loop<MODE>(p, s, rank);
+        producer_loop<MODE>(p, c, s, rank);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (rank == 0 && ptx::elect_one()) {
       if constexpr (MODE == MODE_DHW)
-        dhw_mma(p, s, tmem_base);
+        dhw_mma(p, c, s, tmem_base);
       else
-        mma_loop<MODE>(p, s, tmem_base);
+        mma_loop<MODE>(p, c, s, tmem_base);
     }
     __syncwarp();
   } else {
     if constexpr (MODE == MODE_DHW)
-      dhw_epilogue(p, s, tmem_base, warp, lane, rank);
+      dhw_epilogue(p, c, s, tmem_base, warp, lane, rank);
     else
-      epilogue_loop<MODE>(p, s, tmem_base, warp, lane, rank);
+      epilogue_loop<MODE>(p, c, s, tmem_base, warp, lane, rank);
   }
 
   // After an abort the odd CTA's loads may not have been consumed (they are
@@ -987,6 +1048,7 @@ __global__ void __launch_bounds__(kReduceThreads) fwd_reduce_kernel(const double
 __global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* dloss, const float* dlogp,
                                                                   const int64_t* targets, int T, int V,
                                                                   int64_t ignore_index, int reduction, float* g,
+                                                                  int32_t* row_index, int32_t* row_count,
                                                                   int32_t* status) {
   __shared__ long long sh_cnt[kReduceThreads];
   long long c = 0;
@@ -1008,14 +1070,82 @@ __global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* d
     __syncthreads();
   }
   const long long n = sh_cnt[0];
+  __syncthreads();
   const float d0 = dloss ? dloss[0] : 0.0f;
   const float scalar = (reduction == 1) ? (n > 0 ? d0 / static_cast<float>(n) : 0.0f) : (reduction == 2 ? d0 : 0.0f);
-  for (int t = threadIdx.x; t < T; t += kReduceThreads) {
-    const int64_t y = targets[t];
-    const bool valid = (y != ignore_index) && y >= 0 && y < V;
-    float gt = reduction == 0 ? (dloss ? dloss[t] : 0.0f) : scalar;
-    if (dlogp) gt -= dlogp[t];
-    g[t] = valid ? gt : 0.0f;
+  // g_t, and the list of the rows whose g_t is not zero (their dZ rows are the only
+  // non-zero ones) in token order: rounds of kReduceThreads consecutive tokens, each
+  // placed by a ballot within its warp and a scan of the 32 warp counts.
+  static_assert(kReduceThreads == 1024, "one warp scans the 32 warp counts");
+  __shared__ int warp_off[kReduceThreads / 32];
+  __shared__ int round_total;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  int base = 0;
+  for (int r0 = 0; r0 < T; r0 += kReduceThreads) {
+    const int t = r0 + static_cast<int>(threadIdx.x);
+    float gt = 0.0f;
+    if (t < T) {
+      const int64_t y = targets[t];
+      const bool valid = (y != ignore_index) && y >= 0 && y < V;
+      gt = reduction == 0 ? (dloss ? dloss[t] : 0.0f) : scalar;
+      if (dlogp) gt -= dlogp[t];
+      gt = valid ? gt : 0.0f;
+      g[t] = gt;
+    }
+    const bool keep = t < T && gt != 0.0f;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) warp_off[warp] = __popc(m);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_off[lane];
+      int inc = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
+      }
+      warp_off[lane] = inc - v;
+      if (lane == 31) round_total = inc;
+    }
+    __syncthreads();
+    if (keep) row_index[base + warp_off[warp] + __popc(m & ((1u << lane) - 1u))] = t;
+    base += round_total;
+    __syncthreads();  // warp_off and round_total are rewritten by the next round
+  }
+  if (threadIdx.x == 0) *row_count = base;
+}
+
+// Rows list positions index0 .. index0 + rows - 1 of H, gathered into the chunk
+// buffer Hc, 16 bytes at a time; Hc rows rows .. min(cap, round_up(rows, 256)) - 1
+// (read by the chunk's last tile pair, and as the K tail of its dW tiles) are zeroed.
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(const uint4* H, const int32_t* row_index,
+                                                                   const int32_t* row_count, int index0, int cap,
+                                                                   int row_vecs, uint4* Hc) {
+  const int rows = min(max(*row_count - index0, 0), cap);
+  const int fill = min(cap, (rows + 2 * BM - 1) / (2 * BM) * (2 * BM));
+  const int64_t n = static_cast<int64_t>(fill) * row_vecs;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n; v += stride) {
+    const int i = static_cast<int>(v / row_vecs);
+    const int j = static_cast<int>(v - static_cast<int64_t>(i) * row_vecs);
+    Hc[v] = i < rows ? H[static_cast<int64_t>(row_index[index0 + i]) * row_vecs + j] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// dH rows of the chunk (list order, in dHc) written back to their tokens' rows.
+__global__ void __launch_bounds__(kCopyThreads) scatter_rows_kernel(const uint4* dHc, const int32_t* row_index,
+                                                                    const int32_t* row_count, int index0, int cap,
+                                                                    int row_vecs, uint4* dH) {
+  const int rows = min(max(*row_count - index0, 0), cap);
+  const int64_t n = static_cast<int64_t>(rows) * row_vecs;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n; v += stride) {
+    const int i = static_cast<int>(v / row_vecs);
+    const int j = static_cast<int>(v - static_cast<int64_t>(i) * row_vecs);
+    dH[static_cast<int64_t>(row_index[index0 + i]) * row_vecs + j] = dHc[v];
   }
 }
 

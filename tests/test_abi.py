@@ -119,3 +119,18 @@ def test_misaligned_typed_arrays_are_rejected_on_the_host(lib):
     assert st == 3                 # shard_zy off by 2
     st = lib.flce_forward_shard(P(16), P(16), P(16), 10, 64, 25, 0, 50, -100, P(16), P(14), P(256), 1 << 20, None)
     assert st == 3
+
+
+def test_backward_workspace_for_a_chunk_round_trips(lib):
+    """flce_backward_workspace_size_for_chunk(c) is the smallest workspace that runs
+    chunks of c rows (capped at T rounded up to 128), on ragged and large shapes."""
+    for T, Hd, V in [(1, 64, 1), (300, 64, 4097), (8192, 2048, 124160), (65536, 4096, 248320)]:
+        cap = -(-T // 128) * 128
+        for c in (128, 256, 4096, 8192, 16384):
+            w = lib.flce_backward_workspace_size_for_chunk(T, Hd, V, c)
+            assert lib.flce_backward_chunk_tokens(T, Hd, V, w) == min(c, cap)
+            assert lib.flce_backward_chunk_tokens(T, Hd, V, w - 1) < min(c, cap)
+        assert lib.flce_backward_chunk_tokens(T, Hd, V, lib.flce_backward_workspace_size(T, Hd, V)) == \
+            min(8192, max(128, T // 2 // 128 * 128))
+    assert lib.flce_backward_workspace_size_for_chunk(1000, 64, 50, 100) == 0   # not a multiple of 128
+    assert lib.flce_backward_workspace_size_for_chunk(1000, 64, 50, 0) == 0

@@ -40,10 +40,8 @@ def test_random_shape(case, cuda_device):
                  else np.array([rng.uniform(0.5, 2.0)], dtype=np.float32))
     ws = None
     if chunk and T > 0:
-        ws = flce.flce_backward_workspace_size(T, Hd, V)
-        while flce.flce_backward_chunk_tokens(T, Hd, V, ws) > chunk:
-            ws -= 2 * 128 * ((V + 63) // 64 * 64)
-        assert flce.flce_backward_chunk_tokens(T, Hd, V, ws) >= 128
+        ws = flce.flce_backward_workspace_size_for_chunk(T, Hd, V, chunk)
+        assert flce.flce_backward_chunk_tokens(T, Hd, V, ws) == min(chunk, -(-T // 128) * 128)
     out = run(inp, cuda_device, bwd_workspace_bytes=ws)
     H64, W64 = inp.H64(), inp.W64()
     ref = oracle.forward(H64, W64, inp.targets, IGNORE_INDEX, red)

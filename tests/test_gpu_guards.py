@@ -68,9 +68,7 @@ def test_no_write_outside_any_buffer(shape, cuda_device):
     dH = Guarded((T, Hd), torch.bfloat16, dev)
     dW = Guarded((V, Hd), torch.float32, dev)
     # a workspace for 128-token chunks: several chunks whenever T > 128
-    bws_bytes = flce.flce_backward_workspace_size(T, Hd, V)
-    while flce.flce_backward_chunk_tokens(T, Hd, V, bws_bytes) > 128:
-        bws_bytes -= 2 * 128 * ((V + 63) // 64 * 64)
+    bws_bytes = flce.flce_backward_workspace_size_for_chunk(T, Hd, V, 128)
     bws = Guarded((bws_bytes,), torch.uint8, dev)
     assert lib.flce_backward(P(dloss.data_ptr()), P(H.data_ptr()), P(W.data_ptr()), P(y.data_ptr()), _p(lse), T, Hd,
                              V, IGNORE_INDEX, 1, _p(dH), _p(dW), _p(bws), bws.nbytes, s) == 0

@@ -62,7 +62,7 @@ def test_many_token_chunks(cuda_device):
     """A workspace sized for 128-token chunks: dW accumulates over 8 chunks in order."""
     inp = generate("medium", T=1000, Hd=256, V=5000)
     ws = flce.flce_backward_workspace_size(1000, 256, 5000)
-    chunk_ws = 5120 + 2 * 128 * 5056
+    chunk_ws = flce.flce_backward_workspace_size_for_chunk(1000, 256, 5000, 128)
     assert flce.flce_backward_chunk_tokens(1000, 256, 5000, chunk_ws) == 128
     assert chunk_ws < ws
     _full_check(inp, run(inp, cuda_device, bwd_workspace_bytes=chunk_ws))
@@ -213,7 +213,8 @@ def test_full_size_workload(name, cuda_device):
     bws_b = flce.flce_backward_workspace_size(T, Hd, V)
     chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_b)
     v_pad = (V + 63) // 64 * 64
-    assert bws_b <= 2 * chunk * v_pad + 4 * T + (1 << 20)
+    # dZ slice [chunk x V], the chunk's H and dH rows [chunk x Hd] each, g and the row list [T]
+    assert bws_b <= 2 * chunk * v_pad + 4 * chunk * Hd + 8 * T + (1 << 20)
     assert fws_b <= (8 * 16 + 4) * (T + 128) + (1 << 20)  # (m, s) per token and vocab range, at most 16 ranges
     io = 2 * T * Hd + 2 * V * Hd + 8 * T + 4 * T + 3 * 4 * T + 8 + 2 * T * Hd + 4 * V * Hd
     assert peak_extra <= io + fws_b + bws_b + (64 << 20)  # caching-allocator rounding
@@ -256,8 +257,7 @@ def test_dz_block_beyond_2_31_elements(cuda_device):
     T, Hd, V = 8192, 64, 300001
     inp = generate("medium", T=T, Hd=Hd, V=V)
     v_pad = (V + 63) // 64 * 64
-    ws = flce.flce_backward_workspace_size(T, Hd, V)
-    ws += 2 * (8192 - flce.flce_backward_chunk_tokens(T, Hd, V, ws)) * v_pad
+    ws = flce.flce_backward_workspace_size_for_chunk(T, Hd, V, 8192)
     assert flce.flce_backward_chunk_tokens(T, Hd, V, ws) == 8192 and 8192 * v_pad > 2 ** 31
     out = run(inp, cuda_device, bwd_workspace_bytes=ws)
     assert out["fwd_status"] == 0 and out["bwd_status"] == 0
@@ -280,6 +280,48 @@ def test_dz_block_beyond_2_31_elements(cuda_device):
     assert abs(lhs - rhs) <= TOL_GRAD * max(abs(lhs), abs(rhs)) + 1e-6
     # the last vocab rows (beyond 2^31 / 8192 columns into the block) carry gradient too
     assert float(dW[-64:].abs().max().item()) > 0.0
+
+
+def test_skipped_rows_do_not_reach_the_gradients(cuda_device):
+    """The backward leaves rows whose upstream weight is zero (here: the masked prompt
+    prefixes of the policy-gradient recipe, 30 % of every sequence) out of its
+    contractions.  With Inf and NaN written into those rows of H, dH and dW are
+    bit-identical to the run with the original rows, the skipped rows of dH are exactly
+    zero, and both runs match the oracle."""
+    inp = generate("rlpg", T=1000, Hd=256, V=5000, n_seq=4)
+    H, W, y, dl = to_device(inp, cuda_device)
+    ign = torch.from_numpy(inp.targets == inp.ignore_index).to(cuda_device)
+    assert 0.2 < float(ign.float().mean().item()) < 0.4
+    H_bad = H.clone()
+    rows = torch.nonzero(ign).flatten()
+    H_bad[rows[0::2]] = float("inf")
+    H_bad[rows[1::2]] = float("nan")
+    outs = []
+    for Hx in (H, H_bad):
+        _, lse, _, _, _ = flce.flce_forward(Hx, W, y, inp.ignore_index, inp.reduction)
+        dH, dW, ws = flce.flce_backward(dl, Hx, W, y, lse, inp.ignore_index, inp.reduction)
+        assert flce.flce_read_device_status(ws) == 0
+        outs.append((dH, dW))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert bool((outs[1][0][ign] == 0).all().item())
+    assert bool(torch.isfinite(outs[1][1]).all().item())
+    dH_ref, dW_ref = oracle.backward(inp.dloss, inp.H64(), inp.W64(), inp.targets, inp.ignore_index, inp.reduction)
+    assert rel_fro(outs[1][0].float().cpu().numpy(), dH_ref) <= TOL_GRAD
+    assert rel_fro(outs[1][1].cpu().numpy(), dW_ref) <= TOL_GRAD
+
+
+def test_zero_upstream_gradient_everywhere(cuda_device):
+    """Reduction none with dloss = 0 on every row: no row is left for the contractions,
+    and dH and dW come out exactly zero (dW from the first chunk's zero fill)."""
+    inp = generate("medium", T=700, Hd=128, V=3000)
+    H, W, y, _ = to_device(inp, cuda_device)
+    _, lse, _, _, _ = flce.flce_forward(H, W, y, inp.ignore_index, "none")
+    dW = torch.full((3000, 128), 7.0, device=cuda_device)
+    dH = torch.full((700, 128), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    _, _, ws = flce.flce_backward(torch.zeros(700, device=cuda_device), H, W, y, lse, inp.ignore_index, "none",
+                                  out={"dH": dH, "dW": dW})
+    assert flce.flce_read_device_status(ws) == 0
+    assert bool((dH == 0).all().item()) and bool((dW == 0).all().item())
 
 
 def test_full_size_sampled_dW_medium(cuda_device):
