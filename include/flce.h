@@ -91,10 +91,10 @@ FLCE_API size_t flce_forward_workspace_size(int64_t T, int64_t Hd, int64_t V);
  * (ignored targets; their dZ rows vanish) and works on chunks of `chunk` of
  * the remaining rows, in token order; the workspace holds one [chunk x V] bf16
  * slice of dZ (the page's [block x vocab] residency), the chunk's rows of H
- * and dH ([chunk x Hd] bf16 each) and O(T) scalars.  The default chunk is
- * min(8192, T/2 rounded down to 128) (128 below T = 256), so for T > 256 and
- * Hd < V/2 the workspace stays below the T*V*2 bytes of one dense bf16 logits
- * tensor.  A larger or smaller workspace is accepted:
+ * and dH ([chunk x Hd] bf16 each) and O(T) scalars.  The default chunk is T
+ * rounded up to 128 for T <= 256, else min(8192, T/2 rounded down to 128), so
+ * for T > 256 and Hd < V/2 the workspace stays below the T*V*2 bytes of one
+ * dense bf16 logits tensor.  A larger or smaller workspace is accepted:
  * the backward then uses the largest chunk (a multiple of 128 rows, at least
  * 128) that fits. */
 FLCE_API size_t flce_backward_workspace_size(int64_t T, int64_t Hd, int64_t V);

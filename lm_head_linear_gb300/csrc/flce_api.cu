@@ -298,10 +298,11 @@ BwdLayout bwd_layout(int64_t T, int64_t Hd, int64_t V, int64_t chunk) {
 }
 
 int64_t default_chunk(int64_t T) {
-  // At most T / 2 whenever T >= 256, so dZ residency stays [chunk x V] <= [T/2 x V],
-  // and the whole workspace below one [T x V] bf16 tensor whenever Hd < V / 2.
-  int64_t c = std::max<int64_t>(T, 0) / 2 / 128 * 128;
-  c = std::max<int64_t>(c, 128);
+  // Up to 256 rows: one chunk (fewest launches).  Above: at most T / 2, so dZ
+  // residency stays [chunk x V] <= [T/2 x V] and the whole workspace below one
+  // [T x V] bf16 tensor whenever Hd < V / 2.
+  if (T <= 256) return T <= 128 ? 128 : 256;
+  const int64_t c = std::max<int64_t>(T / 2 / 128 * 128, 128);
   return std::min<int64_t>(c, kDefaultChunk);
 }
 
