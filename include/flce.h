@@ -5,12 +5,13 @@
  * to MI300X", section 3 "Linear cross-entropy: don't build a 32 GB tensor to
  * get a scalar"): the language-model head forms logits Z = H W^T over
  * [tokens x vocab] and reduces every row through the softmax to a per-token
- * cross-entropy.  The fused method never stores Z: it tiles the token axis,
- * forms each logit tile on the fly and folds it into a running maximum and
- * log-sum-exp, keeping only a few scalars per row.  The backward recomputes
- * each logit tile, forms dZ = softmax(Z) - onehot(target) (scaled by the
- * upstream per-token gradient) and contracts it at once into dH = dZ W and
- * dW = dZ^T H, so only a [block x vocab] slice of dZ is ever resident.
+ * cross-entropy.  The fused method never stores Z: tokens are processed in
+ * blocks, each block's logits are formed tile by tile and merged straight
+ * into a per-row maximum and sum of exponentials, so a row keeps a handful of
+ * scalars.  The backward forms the same logit tiles again, turns them into
+ * dZ = softmax(Z) - onehot(target) (scaled by the upstream per-token gradient)
+ * and contracts dZ into dH = dZ W and dW = dZ^T H, so no more than a
+ * [block x vocab] slice of dZ exists at a time.
  * Section 2.3, Step 1 of "让长序列 MoE RL 训练更好调：Megatron-Lite / bumblebee
  * 的优化实践" describes the same loss as streaming along the vocab dimension.
  *
