@@ -177,6 +177,7 @@ bool g_prof_on = false;
 std::vector<LaunchRecord> g_records;
 std::vector<cudaEvent_t> g_event_pool;
 
+// An event from the pool, or a new one; nullptr if none can be created.
 cudaEvent_t take_event() {
   if (!g_event_pool.empty()) {
     cudaEvent_t e = g_event_pool.back();
@@ -184,7 +185,7 @@ cudaEvent_t take_event() {
     return e;
   }
   cudaEvent_t e = nullptr;
-  cudaEventCreate(&e);
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
   return e;
 }
 
@@ -212,10 +213,27 @@ struct KernelScope {
     rec.bytes_per_row = bytes_per_row;
     rec.start = take_event();
     rec.stop = take_event();
-    cudaEventRecord(rec.start, s);
+    if (!rec.start || !rec.stop || cudaEventRecord(rec.start, s) != cudaSuccess) {
+      // no timing for this launch (the profile is an aid; the launch itself goes
+      // ahead, and the failed call's error is cleared so that it is not taken for
+      // the launch's)
+      (void)cudaGetLastError();
+      release_events();
+    }
   }
   ~KernelScope() {
     if (nvtx) nvtxRangePop();
+    if (on) {  // an error return before done(): the events go back to the pool
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      release_events();
+    }
+  }
+  // Caller holds g_prof_mu.
+  void release_events() {
+    if (rec.start) g_event_pool.push_back(rec.start);
+    if (rec.stop) g_event_pool.push_back(rec.stop);
+    rec.start = rec.stop = nullptr;
+    on = false;
   }
   void done() {
     if (nvtx) {
@@ -223,10 +241,15 @@ struct KernelScope {
       nvtx = false;
     }
     if (!on) return;
-    cudaEventRecord(rec.stop, stream);
+    const bool ok = cudaEventRecord(rec.stop, stream) == cudaSuccess;
+    if (!ok) (void)cudaGetLastError();
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    g_records.push_back(rec);
-    on = false;
+    if (ok) {
+      g_records.push_back(rec);
+      on = false;
+    } else {
+      release_events();
+    }
   }
 };
 
