@@ -128,6 +128,15 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def clocks_rejected(c):
+    """True for a clock record the timing rules reject: hardware or thermal slowdown, or
+    a median SM clock far below the maximum with no throttle reason active."""
+    if set(c.get("reasons", [])) & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}:
+        return True
+    sm, mx = c.get("sm_mhz"), c.get("sm_max_mhz")
+    return bool(sm and mx and not c.get("reasons") and sm < 0.7 * mx)
+
+
 def reduce_max(x, device=None):
     """Max of a float over the ranks of the default process group (x itself when
     there is none).  NCCL reduces a tensor on `device`, gloo one on the CPU."""
@@ -462,28 +471,37 @@ def run_ours(args):
         for _ in range(args.warmup):
             graph.replay()
         barrier()
-    flce.flce_profile_collect()
-    flce.flce_profile_enable(graph is None)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index) as clocks:
-        barrier()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
-                step()
-        ev1.record(stream)
-        barrier()
-    flce.flce_profile_enable(False)
-    if graph is not None:
-        flce.flce_profile_enable(True)
-        for _ in range(args.steps):
-            step()
+    def timed_region():
+        flce.flce_profile_collect()
+        flce.flce_profile_enable(graph is None)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(dev.index) as sampler:
+            barrier()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    step()
+            ev1.record(stream)
+            barrier()
         flce.flce_profile_enable(False)
-    kstats = flce.flce_profile_collect()
-    ms_total = max_over_ranks(ev0.elapsed_time(ev1))
+        if graph is not None:
+            flce.flce_profile_enable(True)
+            for _ in range(args.steps):
+                step()
+            flce.flce_profile_enable(False)
+        return max_over_ranks(ev0.elapsed_time(ev1)), flce.flce_profile_collect(), sampler.summary()
+
+    # A run whose clocks show a hardware or thermal slowdown, or an SM clock stuck well
+    # below its maximum with no reason given (a clock lock left by someone else), is
+    # measured once more; the line then reports the second run and the first one's clocks.
+    ms_total, kstats, clocks = timed_region()
+    if max_over_ranks(1.0 if clocks_rejected(clocks) else 0.0) > 0.0:  # every rank takes the same branch
+        first = clocks
+        ms_total, kstats, clocks = timed_region()
+        clocks = dict(clocks, remeasured_after=first)
     ms_step = ms_total / args.steps
     value = whole_job_tokens_per_s(T * args.steps, world, ms_total)
     gpu_launches = sum(v["launches"] for v in kstats.values())
@@ -587,7 +605,7 @@ def run_ours(args):
         "kernels": kernels,
         "gpu_launches": int(gpu_launches),
         "e2e": e2e,
-        "clocks": clocks.summary(),
+        "clocks": clocks,
         "memory": memory,
     }
     if args.path == "loss":
