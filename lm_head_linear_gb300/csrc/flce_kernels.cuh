@@ -103,8 +103,8 @@ struct GemmParams {
   int32_t num_k_blocks;
   int32_t n_split;       // MODE_FWD: vocab ranges per token block
   int32_t num_units;
-  int32_t row0;          // first token of the chunk (0 for MODE_FWD)
-  int32_t rows;          // tokens in the chunk (T for MODE_FWD)
+  int32_t row0;          // first row of the launch in the A / B2 operand maps (0 for MODE_FWD)
+  int32_t rows;          // rows of the launch (T for MODE_FWD); over a row list: the chunk's capacity
   int32_t T;
   int32_t V;
   int32_t part_stride;   // MODE_FWD: row stride of one split's partials
