@@ -380,7 +380,28 @@ class VocabSplitPath:
         return 2 * self.chunk * ((self.bounds[0][1] - self.bounds[0][0] + 63) // 64 * 64)
 
 
-PATHS = {"loss": LossPath, "score": ScorePath, "vocab-split": VocabSplitPath}
+class TrainPath(LossPath):
+    """flce_forward_valid + flce_backward: rows with an ignored target skip the forward's
+    contraction too (their lse is not computed); what the autograd wrapper runs."""
+
+    name = "train"
+
+    def __init__(self, flce, torch, inp, wl, dev, args):
+        super().__init__(flce, torch, inp, wl, dev, args)
+        T, Hd, V = inp.T, inp.Hd, inp.V
+        self.metric = "fused linear-CE fwd+bwd tokens/s, masked rows skipped in the forward as well"
+        n_valid = int(np.count_nonzero(inp.targets != inp.ignore_index))
+        self.flops_executed_per_step = (2.0 * n_valid + 6.0 * kept_rows(inp, wl)) * Hd * V
+        self.fws = torch.empty(flce.flce_forward_valid_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
+
+    def step(self, ins, outs):
+        H, W, y, dl = ins
+        f, ign, red = self.flce, self.inp.ignore_index, self.wl.reduction
+        f.flce_forward_valid(H, W, y, ign, red, workspace=self.fws, out=outs)
+        f.flce_backward(dl, H, W, y, outs["lse"], ign, red, workspace=self.bws, out=outs)
+
+
+PATHS = {"loss": LossPath, "train": TrainPath, "score": ScorePath, "vocab-split": VocabSplitPath}
 
 
 def kept_rows(inp, wl):
@@ -633,8 +654,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of one step")
     ap.add_argument("--path", choices=sorted(PATHS), default="loss",
-                    help="loss: flce_forward + flce_backward (the default); score: flce_score alone; "
-                         "vocab-split: the shard entry points over --shards equal vocab shards")
+                    help="loss: flce_forward + flce_backward (the default); train: flce_forward_valid + "
+                         "flce_backward; score: flce_score alone; vocab-split: the shard entry points over "
+                         "--shards equal vocab shards")
     ap.add_argument("--shards", type=int, default=2, help="vocab shards of --path vocab-split")
     ap.add_argument("--bwd-chunk", type=int, default=0,
                     help="backward token chunk (a multiple of 128; default: the library's default workspace)")

@@ -125,11 +125,30 @@ FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* t
                                   float* logp, int64_t* n_valid, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
+/* Forward for training: the same arguments and results as flce_forward(),
+ * except that rows with an ignored target are left out of the contraction
+ * altogether (their lse is written as 0; their loss and logp are 0 as always).
+ * The rows with a valid target are listed in token order, their rows of H
+ * gathered into the workspace, and the logit tiles run over that list only,
+ * so masked tokens (padding, prompt prefixes) cost nothing but the copy; loss,
+ * logp and the lse of listed rows are bit-identical to flce_forward()'s.  The
+ * lse it returns is what flce_backward() needs (the backward reads it only on
+ * rows with a non-zero upstream weight, which are valid rows).
+ *   workspace, workspace_bytes  >= flce_forward_valid_workspace_size(T, Hd, V)
+ *                               (the forward's, plus 8 bytes per token and the
+ *                               [T x Hd] bf16 rows of H) */
+FLCE_API size_t flce_forward_valid_workspace_size(int64_t T, int64_t Hd, int64_t V);
+FLCE_API flce_status flce_forward_valid(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd,
+                                        int64_t V, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
+                                        float* logp, int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* Backward.  Source: section 3 of the first page (recompute the logit tile,
  * form dZ = softmax - onehot for it, contract it into dH and dW at once).
  *   dloss    [1] fp32 (MEAN, SUM) or [T] fp32 (NONE): gradient of the loss output
  *   H, W, targets, T, Hd, V, ignore_index, reduction: as passed to flce_forward
- *   lse      [T] fp32                  the lse output of flce_forward for these inputs
+ *   lse      [T] fp32                  the lse output of flce_forward (or flce_forward_valid)
+ *                                      for these inputs
  *   dH       [T, Hd] bf16              overwritten with dL/dH (fp32 accumulation, rounded)
  *   dW       [V, Hd] fp32              overwritten with dL/dW, accumulated in fp32 over
  *                                      token chunks in a fixed order
@@ -297,7 +316,8 @@ typedef enum flce_kernel_kind {
   FLCE_KERNEL_BWD_DH_DW = 5,      /* dH chunk = dZ W and dW (+)= dZ^T H, one launch per chunk */
   FLCE_KERNEL_BWD_GATHER = 6,     /* the chunk's rows of H gathered through the row list */
   FLCE_KERNEL_BWD_SCATTER = 7,    /* the chunk's dH rows written back to their tokens */
-  FLCE_KERNEL_KINDS = 8
+  FLCE_KERNEL_FWD_LIST = 8,       /* flce_forward_valid: the list of rows with a valid target */
+  FLCE_KERNEL_KINDS = 9
 } flce_kernel_kind;
 
 FLCE_API void flce_profile_enable(int32_t on);

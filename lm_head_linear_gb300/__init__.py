@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     flce_combine_shards,
     flce_backward_workspace_size,
     flce_forward,
+    flce_forward_valid,
+    flce_forward_valid_workspace_size,
     flce_forward_shard,
     flce_forward_workspace_size,
     flce_profile_collect,

@@ -22,7 +22,7 @@ STATUS_NAMES = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_ALIGNMENT",
     4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
 }
-KERNEL_KINDS = 8
+KERNEL_KINDS = 9
 
 # Every symbol the header declares: name -> (restype, argtypes).
 _P = ctypes.c_void_p
@@ -31,9 +31,11 @@ _I32 = ctypes.c_int32
 SIGNATURES = {
     "flce_forward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "flce_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "flce_forward_valid_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "flce_backward_workspace_size_for_chunk": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "flce_backward_chunk_tokens": (_I64, [_I64, _I64, _I64, ctypes.c_size_t]),
     "flce_forward": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_forward_valid": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P]),
     "flce_score_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "flce_score": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -181,6 +183,24 @@ def flce_forward(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore
     a 1-element int64 tensor.  ``out`` may hold preallocated ``loss``, ``lse``,
     ``logp`` and ``n_valid`` tensors.
     """
+    return _forward("flce_forward", "flce_forward_workspace_size", H, W, targets, ignore_index, reduction,
+                    workspace, stream, out)
+
+
+def flce_forward_valid(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+                       reduction: str = "mean", workspace: Optional[torch.Tensor] = None, stream=None,
+                       out: Optional[dict] = None):
+    """Run ``flce_forward_valid``: as :func:`flce_forward`, but rows with an ignored
+    target are not computed (their lse is 0).  Same return values."""
+    return _forward("flce_forward_valid", "flce_forward_valid_workspace_size", H, W, targets, ignore_index,
+                    reduction, workspace, stream, out)
+
+
+def flce_forward_valid_workspace_size(T: int, Hd: int, V: int) -> int:
+    return int(load_library().flce_forward_valid_workspace_size(T, Hd, V))
+
+
+def _forward(entry, size_fn, H, W, targets, ignore_index, reduction, workspace, stream, out):
     _check_inputs(H, W, targets)
     lib = load_library()
     T, Hd = H.shape
@@ -191,10 +211,10 @@ def flce_forward(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore
     lse = _out(out, "lse", T, torch.float32, dev)
     logp = _out(out, "logp", T, torch.float32, dev)
     n_valid = _out(out, "n_valid", 1, torch.int64, dev)
-    need = lib.flce_forward_workspace_size(T, Hd, V)
+    need = getattr(lib, size_fn)(T, Hd, V)
     ws = _workspace(need, dev, workspace)
-    st = lib.flce_forward(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), red, _ptr(loss), _ptr(lse),
-                          _ptr(logp), _ptr(n_valid), _ptr(ws), ws.numel(), _stream_handle(stream))
+    st = getattr(lib, entry)(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), red, _ptr(loss),
+                             _ptr(lse), _ptr(logp), _ptr(n_valid), _ptr(ws), ws.numel(), _stream_handle(stream))
     _check(st)
     return loss, lse, logp, n_valid, ws
 
@@ -370,8 +390,9 @@ def flce_profile_collect() -> dict:
 
 
 class LinearCrossEntropy(torch.autograd.Function):
-    """autograd wrapper: forward runs ``flce_forward``, backward ``flce_backward``
-    (``flce_backward_logp`` when a gradient reaches ``logp``).
+    """autograd wrapper: forward runs ``flce_forward_valid`` (rows with an ignored target
+    cost nothing), backward ``flce_backward`` (``flce_backward_logp`` when a gradient
+    reaches ``logp``).
 
     Returns ``(loss, logp)``; both are differentiable, so an objective built
     from the per-token log-probabilities (e.g. ``-(adv * logp).sum()``) works.
@@ -380,7 +401,7 @@ class LinearCrossEntropy(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, H, W, targets, ignore_index: int = -100, reduction: str = "mean"):
-        loss, lse, logp, _, _ = flce_forward(H, W, targets, ignore_index, reduction)
+        loss, lse, logp, _, _ = flce_forward_valid(H, W, targets, ignore_index, reduction)
         ctx.save_for_backward(H, W, targets, lse)
         ctx.ignore_index = ignore_index
         ctx.reduction = reduction

@@ -285,6 +285,27 @@ FwdLayout fwd_layout(int64_t T, int n_split) {
   return L;
 }
 
+// flce_forward_valid: the forward layout (all kMaxSplit ranges), then the row
+// list [T] and each token's list position [T] (int32), then the listed rows of
+// H [T, Hd] bf16.  The list length sits in the header.
+struct FwdValidLayout {
+  size_t idx_off, pos_off, hc_off, total;
+};
+
+FwdValidLayout fwd_valid_layout(int64_t T, int64_t Hd) {
+  FwdValidLayout L{};
+  const size_t t1 = static_cast<size_t>(std::max<int64_t>(T, 1));
+  size_t off = align_up(fwd_layout(T, kMaxSplit).total, 256);
+  L.idx_off = off;
+  off = align_up(off + sizeof(int32_t) * t1, 256);
+  L.pos_off = off;
+  off = align_up(off + sizeof(int32_t) * t1, 1024);
+  L.hc_off = off;
+  off = align_up(off + 2ull * t1 * static_cast<size_t>(Hd), 256);
+  L.total = off;
+  return L;
+}
+
 struct BwdLayout {
   int64_t chunk;
   int64_t v_pad;
@@ -399,10 +420,13 @@ flce_status static_scratch_address(void** out) {
 // logit (when these rows own the target) go to the workspace layout L.
 // With `best_val` / `best_idx` set (scoring), the argmax variant also records
 // each row's largest logit and its global id per vocab range.
+// Over a row list (rows_dev, row_index set), H holds the listed rows in list
+// order and the partials are written at list positions.
 flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, const void* W, const int64_t* targets,
                               int64_t T, int64_t Hd, int64_t V, int64_t vocab_offset, int64_t ignore_index,
                               uint8_t* ws, FwdLayout* L_out, float* best_val = nullptr,
-                              int32_t* best_idx = nullptr) {
+                              int32_t* best_idx = nullptr, const int32_t* rows_dev = nullptr,
+                              const int32_t* row_index = nullptr) {
   flce_status st;
   const int64_t m_pairs = cdiv(T, 2 * BM);
   const int64_t n_blocks = cdiv(V, BN);
@@ -431,10 +455,15 @@ flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, co
   p.best_idx = best_idx;
   p.status = reinterpret_cast<int32_t*>(ws);
   p.timeout_ns = wait_limit_ns(Hd);
+  p.rows_dev = rows_dev;
+  p.row_index = row_index;
   const bool score = best_val != nullptr;
   const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[score ? MODE_SCORE : MODE_FWD], p.num_units));
-  KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, 2.0 * T * Hd * V,
-                 2.0 * (T * Hd + V * Hd) + (score ? 16.0 : 8.0) * n_split * T + 4.0 * T);
+  // Over a row list the work is counted on the listed rows (read at collection).
+  const double per_row_bytes = 2.0 * Hd + (score ? 16.0 : 8.0) * n_split + 4.0;
+  KernelScope ks(FLCE_KERNEL_FWD_LOGITS_LSE, s, rows_dev ? 0.0 : 2.0 * T * Hd * V,
+                 2.0 * V * Hd + (rows_dev ? 0.0 : per_row_bytes * T), rows_dev, 0, T, rows_dev ? 2.0 * Hd * V : 0.0,
+                 rows_dev ? per_row_bytes : 0.0);
   if (score)
     gemm_kernel<MODE_SCORE><<<grid, kThreads, smem_bytes_for(MODE_SCORE), s>>>(p);
   else
@@ -448,7 +477,7 @@ flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, co
 // Partials of layout L (n_split ranges, z_y) -> lse, logp, loss, n_valid.
 flce_status launch_finalize_reduce(cudaStream_t s, uint8_t* ws, const FwdLayout& L, const int64_t* targets, int64_t T,
                                    int64_t V_total, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
-                                   float* logp, int64_t* n_valid) {
+                                   float* logp, int64_t* n_valid, const int32_t* pos = nullptr) {
   flce_status st;
   FinalizeParams f;
   f.partials = reinterpret_cast<const float2*>(ws + L.partials_off);
@@ -460,6 +489,7 @@ flce_status launch_finalize_reduce(cudaStream_t s, uint8_t* ws, const FwdLayout&
   f.block_sum = reinterpret_cast<double*>(ws + L.bsum_off);
   f.block_count = reinterpret_cast<int64_t*>(ws + L.bcnt_off);
   f.status = reinterpret_cast<int32_t*>(ws);
+  f.pos = pos;
   f.ignore_index = ignore_index;
   f.T = static_cast<int32_t>(T);
   f.V = static_cast<int32_t>(V_total);
@@ -687,6 +717,7 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_KERNEL_BWD_DH_DW: return "bwd_dh_dw";
     case FLCE_KERNEL_BWD_GATHER: return "bwd_gather";
     case FLCE_KERNEL_BWD_SCATTER: return "bwd_scatter";
+    case FLCE_KERNEL_FWD_LIST: return "fwd_list";
     default: return "unknown";
   }
 }
@@ -822,6 +853,66 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* targets, i
   FwdLayout L;
   if ((st = launch_logits_lse(dev, s, H, W, targets, T, Hd, V, 0, ignore_index, ws, &L)) != FLCE_OK) return st;
   return launch_finalize_reduce(s, ws, L, targets, T, V, ignore_index, reduction, loss, lse, logp, n_valid);
+}
+
+size_t flce_forward_valid_workspace_size(int64_t T, int64_t Hd, int64_t V) {
+  if (T < 0 || V < 1 || Hd < 1) return 0;
+  return fwd_valid_layout(T, Hd).total;
+}
+
+flce_status flce_forward_valid(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd,
+                               int64_t V, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
+                               float* logp, int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
+  if (st != FLCE_OK) return st;
+  if (!loss || (T > 0 && (!lse || !logp))) return fail(FLCE_ERR_INVALID_ARG, "loss, lse or logp is NULL");
+  if (misaligned(loss) || misaligned(lse) || misaligned(logp) || misaligned(n_valid))
+    return fail(FLCE_ERR_ALIGNMENT, "loss, lse, logp (4 bytes) or n_valid (8 bytes) misaligned");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (workspace_bytes < flce_forward_valid_workspace_size(T, Hd, V))
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
+                flce_forward_valid_workspace_size(T, Hd, V));
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  if (T == 0) {
+    if (reduction != FLCE_REDUCTION_NONE) CUDA_TRY(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    if (n_valid) CUDA_TRY(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
+    return FLCE_OK;
+  }
+  const FwdValidLayout LV = fwd_valid_layout(T, Hd);
+  int32_t* row_index = reinterpret_cast<int32_t*>(ws + LV.idx_off);
+  int32_t* pos = reinterpret_cast<int32_t*>(ws + LV.pos_off);
+  int32_t* row_count = reinterpret_cast<int32_t*>(ws + kRowCountOff);
+  void* Hc = ws + LV.hc_off;
+  {
+    KernelScope ks(FLCE_KERNEL_FWD_LIST, s, 0.0, 16.0 * T);
+    fwd_list_kernel<<<1, kReduceThreads, 0, s>>>(targets, static_cast<int>(T), static_cast<int>(V), ignore_index,
+                                                 row_index, pos, row_count, reinterpret_cast<int32_t*>(ws));
+    ks.done();
+    if ((st = check_launch("fwd_list")) != FLCE_OK) return st;
+  }
+  {
+    const int row_vecs = static_cast<int>(Hd / 8);
+    const int grid =
+        static_cast<int>(std::min<int64_t>(cdiv(T * row_vecs, kCopyThreads), 8 * static_cast<int64_t>(dev->sms)));
+    KernelScope ks(FLCE_KERNEL_BWD_GATHER, s, 0.0, 0.0, row_count, 0, T, 0.0, 4.0 * Hd + 4.0);
+    gather_rows_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(H), row_index, row_count, 0,
+                                                     static_cast<int>(T), row_vecs, static_cast<uint4*>(Hc));
+    ks.done();
+    if ((st = check_launch("fwd_gather")) != FLCE_OK) return st;
+  }
+  FwdLayout L;
+  if ((st = launch_logits_lse(dev, s, Hc, W, targets, T, Hd, V, 0, ignore_index, ws, &L, nullptr, nullptr, row_count,
+                              row_index)) != FLCE_OK)
+    return st;
+  return launch_finalize_reduce(s, ws, L, targets, T, V, ignore_index, reduction, loss, lse, logp, n_valid, pos);
 }
 
 size_t flce_score_workspace_size(int64_t T, int64_t Hd, int64_t V) {

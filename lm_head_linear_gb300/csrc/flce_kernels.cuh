@@ -124,11 +124,12 @@ struct GemmParams {
   int32_t* tile_counter; // MODE_DHW: zero before the launch
   int32_t* status;
   uint64_t timeout_ns;
-  // MODE_DZ / MODE_DHW over compacted rows (the backward skips rows whose upstream
-  // gradient is zero): the chunk holds list positions index0 .. index0 + rows - 1 of
-  // the row list, whose length the prep kernel writes to *rows_dev; token rows of
-  // H / dH come gathered in the chunk's own buffers, and targets, lse and g are
-  // read through row_index.  rows_dev == nullptr: rows row0 .. row0 + rows - 1.
+  // Over a list of rows (the backward skips rows whose upstream gradient is zero;
+  // the forward of flce_forward_valid skips rows with an ignored target): the launch
+  // holds list positions index0 .. index0 + rows - 1 of the row list, whose length a
+  // prep kernel writes to *rows_dev; token rows of H / dH come gathered in buffers
+  // of their own, and targets, lse and g are read through row_index.
+  // rows_dev == nullptr: rows row0 .. row0 + rows - 1.
   const int32_t* rows_dev;
   const int32_t* row_index;
   int32_t index0;
@@ -146,6 +147,7 @@ struct Counts {
   int num_k_blocks2;  // MODE_DHW: K blocks of a dW tile
 };
 
+template <int MODE>
 __device__ __forceinline__ Counts counts_of(const GemmParams& p) {
   Counts c;
   if (!p.rows_dev) {
@@ -158,7 +160,7 @@ __device__ __forceinline__ Counts counts_of(const GemmParams& p) {
   }
   c.rows = min(max(*p.rows_dev - p.index0, 0), p.rows);
   c.num_m_pairs = (c.rows + 2 * BM - 1) / (2 * BM);
-  c.num_units = c.num_m_pairs * p.num_n_blocks;
+  c.num_units = c.num_m_pairs * (is_forward(MODE) ? p.n_split : p.num_n_blocks);
   c.n_dh_tiles = c.num_m_pairs * p.num_n_blocks;
   c.num_k_blocks2 = (c.rows + BK - 1) / BK;
   return c;
@@ -545,8 +547,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const Counts&
     // y: the target's local vocab column when this launch's vocab rows own it, else -1
     if constexpr (is_forward(MODE)) {
       if (t_local < c.rows) {
-        const int64_t yy = p.targets[t_local] - p.vocab_offset;
-        if (p.targets[t_local] != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
+        const int64_t target = p.targets[p.row_index ? p.row_index[t_local] : t_local];
+        const int64_t yy = target - p.vocab_offset;
+        if (target != p.ignore_index && yy >= 0 && yy < p.V) y = static_cast<int>(yy);
       }
     } else {
       if (t_local < c.rows) {
@@ -759,7 +762,7 @@ template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const Counts c = counts_of(p);
+  const Counts c = counts_of<MODE>(p);
   if (p.rows_dev && c.rows == 0) {
     // An empty chunk of the row list: nothing to compute.  Every CTA sees the same
     // count and leaves before any barrier, TMEM or cluster operation.  When the
@@ -879,6 +882,7 @@ struct FinalizeParams {
   double* block_sum;     // [num_blocks]
   int64_t* block_count;  // [num_blocks]
   int32_t* status;
+  const int32_t* pos;    // row-list position of each token, -1 when not listed; nullptr: position t
   int64_t ignore_index;
   int32_t T;
   int32_t V;
@@ -892,12 +896,18 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(const Fi
   const int t = blockIdx.x * kFinalizeThreads + threadIdx.x;
   double my_loss = 0.0;
   long long my_cnt = 0;
-  if (t < p.T) {
+  const int i = (t < p.T && p.pos) ? p.pos[t] : t;  // the row's slot in the partials
+  if (t < p.T && i < 0) {
+    // not listed (an ignored target): nothing was computed for the row
+    p.lse[t] = 0.0f;
+    p.logp[t] = 0.0f;
+    if (p.loss_rows) p.loss_rows[t] = 0.0f;
+  } else if (t < p.T) {
     float M = -INFINITY;
-    for (int sp = 0; sp < p.n_split; ++sp) M = fmaxf(M, p.partials[static_cast<size_t>(sp) * p.part_stride + t].x);
+    for (int sp = 0; sp < p.n_split; ++sp) M = fmaxf(M, p.partials[static_cast<size_t>(sp) * p.part_stride + i].x);
     float S = 0.0f;
     for (int sp = 0; sp < p.n_split; ++sp) {
-      const float2 pr = p.partials[static_cast<size_t>(sp) * p.part_stride + t];
+      const float2 pr = p.partials[static_cast<size_t>(sp) * p.part_stride + i];
       S += pr.y * exp2f(pr.x - M);
     }
     const float lse = (M + log2f(S)) * kLn2;
@@ -909,7 +919,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(const Fi
     }
     float loss_t = 0.0f, logp_t = 0.0f;
     if (valid) {
-      const float z = p.zy[t];
+      const float z = p.zy[i];
       loss_t = lse - z;
       logp_t = z - lse;
       my_loss = static_cast<double>(loss_t);
@@ -1113,6 +1123,59 @@ __global__ void __launch_bounds__(kReduceThreads) bwd_prep_kernel(const float* d
     base += round_total;
     __syncthreads();  // warp_off and round_total are rewritten by the next round
   }
+  if (threadIdx.x == 0) *row_count = base;
+}
+
+// The list of rows with a valid target, in token order, for flce_forward_valid:
+// row_index[position] = token, pos[token] = position or -1, *row_count = length.
+// Rounds of kReduceThreads tokens, placed by warp ballots and a scan of the
+// warp counts.  A target outside [0, V) that is not ignore_index is flagged
+// and the row left out.
+__global__ void __launch_bounds__(kReduceThreads) fwd_list_kernel(const int64_t* targets, int T, int V,
+                                                                  int64_t ignore_index, int32_t* row_index,
+                                                                  int32_t* pos, int32_t* row_count,
+                                                                  int32_t* status) {
+  static_assert(kReduceThreads == 1024, "one warp scans the 32 warp counts");
+  __shared__ int warp_off[kReduceThreads / 32];
+  __shared__ int round_total;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  int base = 0;
+  bool bad = false;
+  for (int r0 = 0; r0 < T; r0 += kReduceThreads) {
+    const int t = r0 + static_cast<int>(threadIdx.x);
+    bool keep = false;
+    if (t < T) {
+      const int64_t y = targets[t];
+      if (y != ignore_index) {
+        keep = y >= 0 && y < V;
+        bad = bad || !keep;
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) warp_off[warp] = __popc(m);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_off[lane];
+      int inc = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
+      }
+      warp_off[lane] = inc - v;
+      if (lane == 31) round_total = inc;
+    }
+    __syncthreads();
+    if (t < T) {
+      const int at = base + warp_off[warp] + __popc(m & ((1u << lane) - 1u));
+      pos[t] = keep ? at : -1;
+      if (keep) row_index[at] = t;
+    }
+    base += round_total;
+    __syncthreads();
+  }
+  if (bad) raise_status(status, kStatusTargetRange);
   if (threadIdx.x == 0) *row_count = base;
 }
 

@@ -64,6 +64,11 @@ def test_no_write_outside_any_buffer(shape, cuda_device):
                             _p(lse), _p(logp), _p(nv), _p(fws), fws.nbytes, s) == 0
     assert lib.flce_forward(P(H.data_ptr()), P(W.data_ptr()), P(y.data_ptr()), T, Hd, V, IGNORE_INDEX, 0,
                             _p(loss_rows), _p(lse), _p(logp), _p(nv), _p(fws), fws.nbytes, s) == 0
+    vws = Guarded((lib.flce_forward_valid_workspace_size(T, Hd, V),), torch.uint8, dev)
+    vlse = Guarded((T,), torch.float32, dev)
+    vlogp = Guarded((T,), torch.float32, dev)
+    assert lib.flce_forward_valid(P(H.data_ptr()), P(W.data_ptr()), P(y.data_ptr()), T, Hd, V, IGNORE_INDEX, 0,
+                                  _p(loss_rows), _p(vlse), _p(vlogp), _p(nv), _p(vws), vws.nbytes, s) == 0
     dloss = torch.ones(1, device=dev)
     dH = Guarded((T, Hd), torch.bfloat16, dev)
     dW = Guarded((V, Hd), torch.float32, dev)
@@ -90,6 +95,7 @@ def test_no_write_outside_any_buffer(shape, cuda_device):
     for name, g in [("loss", loss), ("loss_rows", loss_rows), ("lse", lse), ("logp", logp), ("n_valid", nv),
                     ("fwd workspace", fws), ("dH", dH), ("dW", dW), ("bwd workspace", bws),
                     ("score workspace", sws), ("argmax", amax), ("shard_lse", slse), ("shard_zy", szy),
-                    ("dH partial", dHp), ("dW shard", dWs)]:
+                    ("dH partial", dHp), ("dW shard", dWs), ("valid-forward workspace", vws),
+                    ("valid-forward lse", vlse), ("valid-forward logp", vlogp)]:
         assert g.intact(), name
     assert flce.flce_read_device_status(fws.t) == 0 and flce.flce_read_device_status(bws.t) == 0
