@@ -134,3 +134,17 @@ def test_backward_workspace_for_a_chunk_round_trips(lib):
         assert lib.flce_backward_chunk_tokens(T, Hd, V, lib.flce_backward_workspace_size(T, Hd, V)) == default
     assert lib.flce_backward_workspace_size_for_chunk(1000, 64, 50, 100) == 0   # not a multiple of 128
     assert lib.flce_backward_workspace_size_for_chunk(1000, 64, 50, 0) == 0
+
+
+def test_size_limits_are_argument_errors(lib):
+    """T and V must stay below 2^30 (tile coordinates stay in int32), Hd below 2^24."""
+    P = ctypes.c_void_p
+    args = lambda T, Hd, V: (P(16), P(16), P(16), T, Hd, V, -100, 1, P(16), P(16), P(16), None, P(256), 1 << 40, None)
+    assert lib.flce_forward(*args(1 << 30, 64, 50)) == 1
+    assert lib.flce_forward(*args(10, 64, 1 << 30)) == 1
+    assert lib.flce_forward(*args(10, 1 << 24, 50)) == 1
+    assert lib.flce_forward(*args(-1, 64, 50)) == 1
+    assert lib.flce_forward(*args(10, 64, 0)) == 1
+    assert lib.flce_forward_valid(*args(1 << 30, 64, 50)) == 1
+    assert lib.flce_backward_workspace_size(-1, 64, 50) == 0
+    assert lib.flce_forward_workspace_size(10, 64, 0) == 0
