@@ -22,26 +22,29 @@ def _buffers(T, Hd, V, dev, reduction):
              "n_valid": torch.empty(1, dtype=torch.int64, device=dev)}
     out_b = {"dH": torch.empty((T, Hd), dtype=torch.bfloat16, device=dev),
              "dW": torch.empty((V, Hd), dtype=torch.float32, device=dev)}
-    fws = torch.empty(flce.flce_forward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
+    fws = torch.empty(max(flce.flce_forward_workspace_size(T, Hd, V), flce.flce_forward_valid_workspace_size(T, Hd, V)),
+                      dtype=torch.uint8, device=dev)
     bws = torch.empty(flce.flce_backward_workspace_size(T, Hd, V), dtype=torch.uint8, device=dev)
     return out_f, out_b, fws, bws
 
 
-def _step(H, W, y, dl, bufs, reduction):
+def _step(H, W, y, dl, bufs, reduction, forward=None):
     out_f, out_b, fws, bws = bufs
-    flce.flce_forward(H, W, y, -100, reduction, workspace=fws, out=out_f)
+    (forward or flce.flce_forward)(H, W, y, -100, reduction, workspace=fws, out=out_f)
     flce.flce_backward(dl, H, W, y, out_f["lse"], -100, reduction, workspace=bws, out=out_b)
 
 
-@pytest.mark.parametrize("shape", [("medium", 1000, 256, 5000), ("tiny", 256, 256, 4096)])
+@pytest.mark.parametrize("shape", [("medium", 1000, 256, 5000, "full"), ("tiny", 256, 256, 4096, "full"),
+                                   ("medium", 1000, 256, 5000, "valid")])
 def test_graph_replay_matches_eager(shape, cuda_device):
-    wl, T, Hd, V = shape
+    wl, T, Hd, V, fwd = shape
+    forward = flce.flce_forward_valid if fwd == "valid" else flce.flce_forward
     a = generate(wl, T=T, Hd=Hd, V=V, seed=1)
     b = generate(wl, T=T, Hd=Hd, V=V, seed=2)
     red = a.reduction
     H, W, y, dl = to_device(a, cuda_device)
     bufs = _buffers(T, Hd, V, cuda_device, red)
-    _step(H, W, y, dl, bufs, red)  # first call on the device: set-up outside the capture
+    _step(H, W, y, dl, bufs, red, forward)  # first call on the device: set-up outside the capture
     torch.cuda.synchronize()
 
     g = torch.cuda.CUDAGraph()
@@ -49,7 +52,7 @@ def test_graph_replay_matches_eager(shape, cuda_device):
     s.wait_stream(torch.cuda.current_stream(cuda_device))
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            _step(H, W, y, dl, bufs, red)
+            _step(H, W, y, dl, bufs, red, forward)
     torch.cuda.current_stream(cuda_device).wait_stream(s)
 
     for inp in (b, a, b):
@@ -62,7 +65,7 @@ def test_graph_replay_matches_eager(shape, cuda_device):
         torch.cuda.synchronize()
         got = {k: v.clone() for d in bufs[:2] for k, v in d.items()}
         ref_bufs = _buffers(T, Hd, V, cuda_device, red)
-        _step(Hn, Wn, yn, dln, ref_bufs, red)
+        _step(Hn, Wn, yn, dln, ref_bufs, red, forward)
         torch.cuda.synchronize()
         for d in ref_bufs[:2]:
             for k, v in d.items():

@@ -42,3 +42,38 @@ def test_two_streams_match_one_stream(cuda_device):
         for k in ("loss", "lse", "logp", "dH", "dW"):
             assert torch.equal(x[k], y[k]), k
         assert flce.flce_read_device_status(y["fws"]) == 0 and flce.flce_read_device_status(y["bws"]) == 0
+
+
+def test_two_host_threads(cuda_device):
+    """Two host threads call the library at the same time (ctypes releases the GIL during
+    the calls), each on its own stream with its own buffers, five steps each: the results
+    match the one-stream results bit for bit."""
+    import threading
+
+    probs = [_problem(21, cuda_device), _problem(22, cuda_device)]
+    s0 = torch.cuda.current_stream(cuda_device)
+    seq = [_call(inp, t, s0) for inp, t in probs]
+    torch.cuda.synchronize()
+    results, errors = [None, None], []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(cuda_device)
+            st = torch.cuda.Stream(cuda_device)
+            st.wait_stream(s0)
+            for _ in range(5):
+                results[i] = _call(probs[i][0], probs[i][1], st)
+            st.synchronize()
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for x, y in zip(seq, results):
+        for k in ("loss", "lse", "logp", "dH", "dW"):
+            assert torch.equal(x[k], y[k]), k
