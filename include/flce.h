@@ -58,7 +58,11 @@
 extern "C" {
 #endif
 
-#define FLCE_ABI_VERSION 1
+/* 1: the first interface.  2: the backward skips rows with a zero upstream
+ * weight (its workspace holds the row list and the chunk's H and dH rows),
+ * flce_forward_valid and flce_backward_workspace_size_for_chunk added,
+ * kernel kinds 6-8 added to the timing aid. */
+#define FLCE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define FLCE_API __attribute__((visibility("default")))

@@ -23,6 +23,7 @@ STATUS_NAMES = {
     4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
 }
 KERNEL_KINDS = 9
+ABI_VERSION = 2  # FLCE_ABI_VERSION of include/flce.h
 
 # Every symbol the header declares: name -> (restype, argtypes).
 _P = ctypes.c_void_p
@@ -91,8 +92,8 @@ def load_library() -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        if lib.flce_abi_version() != 1:
-            raise RuntimeError("libflce ABI version mismatch")
+        if lib.flce_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"libflce ABI version {lib.flce_abi_version()}, this binding needs {ABI_VERSION}")
         _LIB = lib
     return _LIB
 

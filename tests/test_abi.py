@@ -49,7 +49,7 @@ def test_exported_symbols_are_only_the_declared_ones(lib):
 
 
 def test_host_only_entry_points(lib):
-    assert lib.flce_abi_version() == 1
+    assert lib.flce_abi_version() == 2
     assert lib.flce_status_string(0) == b"FLCE_OK"
     assert lib.flce_status_string(6) == b"FLCE_ERR_TARGET_RANGE"
     assert lib.flce_kernel_name(4) == b"bwd_dz"
@@ -148,3 +148,12 @@ def test_size_limits_are_argument_errors(lib):
     assert lib.flce_forward_valid(*args(1 << 30, 64, 50)) == 1
     assert lib.flce_backward_workspace_size(-1, 64, 50) == 0
     assert lib.flce_forward_workspace_size(10, 64, 0) == 0
+
+
+def test_binding_and_header_agree_on_the_abi_version():
+    import re
+
+    import lm_head_linear_gb300.binding as b
+    with open(os.path.join(ROOT, "include", "flce.h")) as fh:
+        m = re.search(r"#define FLCE_ABI_VERSION (\d+)", fh.read())
+    assert m and int(m.group(1)) == b.ABI_VERSION
