@@ -401,7 +401,27 @@ class TrainPath(LossPath):
         f.flce_backward(dl, H, W, y, outs["lse"], ign, red, workspace=self.bws, out=outs)
 
 
-PATHS = {"loss": LossPath, "train": TrainPath, "score": ScorePath, "vocab-split": VocabSplitPath}
+class ScoreValidPath(ScorePath):
+    """flce_score_valid: scoring over the rows with a valid target only."""
+
+    name = "score-valid"
+
+    def __init__(self, flce, torch, inp, wl, dev, args):
+        super().__init__(flce, torch, inp, wl, dev, args)
+        T, Hd, V = inp.T, inp.Hd, inp.V
+        self.metric = "scoring tokens/s over the rows with a valid target (masked rows skipped)"
+        self.flops_executed_per_step = 2.0 * int(np.count_nonzero(inp.targets != inp.ignore_index)) * Hd * V
+        lib = flce.load_library()
+        self.ws = torch.empty(max(lib.flce_score_valid_workspace_size(T, Hd, V), 256), dtype=torch.uint8,
+                              device=dev)
+
+    def step(self, ins, outs):
+        H, W, y = ins
+        self.flce.flce_score_valid(H, W, y, self.inp.ignore_index, workspace=self.ws, out=outs)
+
+
+PATHS = {"loss": LossPath, "train": TrainPath, "score": ScorePath, "score-valid": ScoreValidPath,
+         "vocab-split": VocabSplitPath}
 
 
 def kept_rows(inp, wl):
@@ -655,8 +675,8 @@ def main():
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of one step")
     ap.add_argument("--path", choices=sorted(PATHS), default="loss",
                     help="loss: flce_forward + flce_backward (the default); train: flce_forward_valid + "
-                         "flce_backward; score: flce_score alone; vocab-split: the shard entry points over "
-                         "--shards equal vocab shards")
+                         "flce_backward; score: flce_score alone; score-valid: flce_score_valid alone; "
+                         "vocab-split: the shard entry points over --shards equal vocab shards")
     ap.add_argument("--shards", type=int, default=2, help="vocab shards of --path vocab-split")
     ap.add_argument("--bwd-chunk", type=int, default=0,
                     help="backward token chunk (a multiple of 128; default: the library's default workspace)")

@@ -60,8 +60,8 @@ extern "C" {
 
 /* 1: the first interface.  2: the backward skips rows with a zero upstream
  * weight (its workspace holds the row list and the chunk's H and dH rows),
- * flce_forward_valid and flce_backward_workspace_size_for_chunk added,
- * kernel kinds 6-8 added to the timing aid. */
+ * flce_forward_valid, flce_score_valid and flce_backward_workspace_size_for_chunk
+ * added, kernel kinds 6-8 added to the timing aid. */
 #define FLCE_ABI_VERSION 2
 
 #if defined(__GNUC__)
@@ -218,6 +218,17 @@ FLCE_API size_t flce_score_workspace_size(int64_t T, int64_t Hd, int64_t V);
 FLCE_API flce_status flce_score(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
                                 int64_t ignore_index, float* logp, float* lse, int64_t* argmax, void* workspace,
                                 size_t workspace_bytes, void* stream);
+
+/* Scoring over the rows with a valid target only: the same arguments and results
+ * as flce_score(), except that rows with an ignored target are left out of the
+ * contraction (lse 0, logp 0 and argmax -1 there); on every other row lse, logp
+ * and argmax are bit-identical to flce_score()'s.  For scoring a rollout's
+ * response tokens with the prompt masked.
+ *   workspace, workspace_bytes  >= flce_score_valid_workspace_size(T, Hd, V) */
+FLCE_API size_t flce_score_valid_workspace_size(int64_t T, int64_t Hd, int64_t V);
+FLCE_API flce_status flce_score_valid(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd,
+                                      int64_t V, int64_t ignore_index, float* logp, float* lse, int64_t* argmax,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- vocab-parallel split ---------------------------------------------------
  * The vocabulary split into shards of consecutive rows, as when the LM head is

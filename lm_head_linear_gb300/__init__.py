@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     flce_profile_enable,
     flce_read_device_status,
     flce_score,
+    flce_score_valid,
     flce_selftest_wait_timeout,
     flce_set_wait_timeout_ns,
     library_path,

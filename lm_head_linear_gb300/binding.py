@@ -39,7 +39,9 @@ SIGNATURES = {
     "flce_forward_valid": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_noalloc": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P]),
     "flce_score_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "flce_score_valid_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "flce_score": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "flce_score_valid": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_forward_shard": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P]),
     "flce_combine_workspace_size": (ctypes.c_size_t, [_I64, _I32]),
     "flce_combine_shards": (_I32, [_P, _P, _I32, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, ctypes.c_size_t,
@@ -266,6 +268,18 @@ def flce_score(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_i
                workspace: Optional[torch.Tensor] = None, stream=None, out: Optional[dict] = None):
     """Run ``flce_score``; returns ``(logp [T] fp32, lse [T] fp32, argmax [T] int64, workspace)``.
     ``out`` may hold preallocated ``logp``, ``lse`` and ``argmax`` tensors."""
+    return _score("flce_score", "flce_score_workspace_size", H, W, targets, ignore_index, workspace, stream, out)
+
+
+def flce_score_valid(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+                     workspace: Optional[torch.Tensor] = None, stream=None, out: Optional[dict] = None):
+    """Run ``flce_score_valid``: as :func:`flce_score` on the rows with a valid target;
+    rows with an ignored target are not computed (lse 0, logp 0, argmax -1)."""
+    return _score("flce_score_valid", "flce_score_valid_workspace_size", H, W, targets, ignore_index, workspace,
+                  stream, out)
+
+
+def _score(entry, size_fn, H, W, targets, ignore_index, workspace, stream, out):
     _check_inputs(H, W, targets)
     lib = load_library()
     T, Hd = H.shape
@@ -274,9 +288,9 @@ def flce_score(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, ignore_i
     logp = _out(out, "logp", T, torch.float32, dev)
     lse = _out(out, "lse", T, torch.float32, dev)
     argmax = _out(out, "argmax", T, torch.int64, dev)
-    ws = _workspace(lib.flce_score_workspace_size(T, Hd, V), dev, workspace)
-    _check(lib.flce_score(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), _ptr(logp), _ptr(lse),
-                          _ptr(argmax), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    ws = _workspace(getattr(lib, size_fn)(T, Hd, V), dev, workspace)
+    _check(getattr(lib, entry)(_ptr(H), _ptr(W), _ptr(targets), T, Hd, V, int(ignore_index), _ptr(logp), _ptr(lse),
+                               _ptr(argmax), _ptr(ws), ws.numel(), _stream_handle(stream)))
     return logp, lse, argmax, ws
 
 

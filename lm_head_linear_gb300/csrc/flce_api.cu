@@ -955,7 +955,88 @@ flce_status flce_score(const void* H, const void* W, const int64_t* targets, int
   score_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(
       reinterpret_cast<const float2*>(ws + L.partials_off), reinterpret_cast<const float*>(ws + L.zy_off), best_val,
       best_idx, targets, static_cast<int>(T), static_cast<int>(V), ignore_index, L.n_split,
-      static_cast<int>(L.part_stride), lse, logp, argmax, reinterpret_cast<int32_t*>(ws));
+      static_cast<int>(L.part_stride), lse, logp, argmax, reinterpret_cast<int32_t*>(ws), nullptr);
+  ks.done();
+  return check_launch("score_finalize");
+}
+
+// flce_score_valid: the scoring workspace, then the row list, the position map
+// and the listed rows of H, as in the flce_forward_valid layout.
+static FwdValidLayout score_valid_layout(int64_t T, int64_t Hd, int64_t V) {
+  FwdValidLayout L{};
+  const size_t t1 = static_cast<size_t>(std::max<int64_t>(T, 1));
+  size_t off = align_up(flce_score_workspace_size(T, Hd, V), 256);
+  L.idx_off = off;
+  off = align_up(off + sizeof(int32_t) * t1, 256);
+  L.pos_off = off;
+  off = align_up(off + sizeof(int32_t) * t1, 1024);
+  L.hc_off = off;
+  off = align_up(off + 2ull * t1 * static_cast<size_t>(Hd), 256);
+  L.total = off;
+  return L;
+}
+
+size_t flce_score_valid_workspace_size(int64_t T, int64_t Hd, int64_t V) {
+  if (T < 0 || V < 1 || Hd < 1) return 0;
+  return score_valid_layout(T, Hd, V).total;
+}
+
+flce_status flce_score_valid(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
+                             int64_t ignore_index, float* logp, float* lse, int64_t* argmax, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, FLCE_REDUCTION_NONE);
+  if (st != FLCE_OK) return st;
+  if (T > 0 && !logp) return fail(FLCE_ERR_INVALID_ARG, "logp is NULL");
+  if (misaligned(logp) || misaligned(lse) || misaligned(argmax))
+    return fail(FLCE_ERR_ALIGNMENT, "logp, lse (4 bytes) or argmax (8 bytes) misaligned");
+  if (!workspace) return fail(FLCE_ERR_WORKSPACE, "workspace is NULL");
+  if (workspace_bytes < flce_score_valid_workspace_size(T, Hd, V))
+    return fail(FLCE_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes,
+                flce_score_valid_workspace_size(T, Hd, V));
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(FLCE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  if ((st = get_encoder()) != FLCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  if (T == 0) return FLCE_OK;
+  const FwdValidLayout LV = score_valid_layout(T, Hd, V);
+  int32_t* row_index = reinterpret_cast<int32_t*>(ws + LV.idx_off);
+  int32_t* pos = reinterpret_cast<int32_t*>(ws + LV.pos_off);
+  int32_t* row_count = reinterpret_cast<int32_t*>(ws + kRowCountOff);
+  void* Hc = ws + LV.hc_off;
+  {
+    KernelScope ks(FLCE_KERNEL_FWD_LIST, s, 0.0, 16.0 * T);
+    fwd_list_kernel<<<1, kReduceThreads, 0, s>>>(targets, static_cast<int>(T), static_cast<int>(V), ignore_index,
+                                                 row_index, pos, row_count, reinterpret_cast<int32_t*>(ws));
+    ks.done();
+    if ((st = check_launch("fwd_list")) != FLCE_OK) return st;
+  }
+  {
+    const int row_vecs = static_cast<int>(Hd / 8);
+    const int grid =
+        static_cast<int>(std::min<int64_t>(cdiv(T * row_vecs, kCopyThreads), 8 * static_cast<int64_t>(dev->sms)));
+    KernelScope ks(FLCE_KERNEL_BWD_GATHER, s, 0.0, 0.0, row_count, 0, T, 0.0, 4.0 * Hd + 4.0);
+    gather_rows_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(H), row_index, row_count, 0,
+                                                     static_cast<int>(T), row_vecs, static_cast<uint4*>(Hc));
+    ks.done();
+    if ((st = check_launch("fwd_gather")) != FLCE_OK) return st;
+  }
+  const FwdLayout Lmax = fwd_layout(T, kMaxSplit);
+  const size_t best_bytes = align_up(sizeof(float) * kMaxSplit * static_cast<size_t>(Lmax.part_stride), 256);
+  float* best_val = reinterpret_cast<float*>(ws + Lmax.total);
+  int32_t* best_idx = reinterpret_cast<int32_t*>(ws + Lmax.total + best_bytes);
+  FwdLayout L;
+  if ((st = launch_logits_lse(dev, s, Hc, W, targets, T, Hd, V, 0, ignore_index, ws, &L, best_val, best_idx,
+                              row_count, row_index)) != FLCE_OK)
+    return st;
+  KernelScope ks(FLCE_KERNEL_FWD_FINALIZE, s, 0.0, (16.0 * L.n_split + 4 + 8 + 4 + 4 + 8) * T);
+  score_finalize_kernel<<<L.num_fin_blocks, kFinalizeThreads, 0, s>>>(
+      reinterpret_cast<const float2*>(ws + L.partials_off), reinterpret_cast<const float*>(ws + L.zy_off), best_val,
+      best_idx, targets, static_cast<int>(T), static_cast<int>(V), ignore_index, L.n_split,
+      static_cast<int>(L.part_stride), lse, logp, argmax, reinterpret_cast<int32_t*>(ws), pos);
   ks.done();
   return check_launch("score_finalize");
 }

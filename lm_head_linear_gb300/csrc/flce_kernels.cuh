@@ -950,16 +950,23 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(const Fi
 __global__ void __launch_bounds__(kFinalizeThreads) score_finalize_kernel(
     const float2* partials, const float* zy, const float* best_val, const int32_t* best_idx, const int64_t* targets,
     int T, int V, int64_t ignore_index, int n_split, int part_stride, float* lse_out, float* logp_out,
-    int64_t* argmax_out, int32_t* status) {
+    int64_t* argmax_out, int32_t* status, const int32_t* pos) {
   const int t = blockIdx.x * kFinalizeThreads + threadIdx.x;
   if (t >= T) return;
+  const int r = pos ? pos[t] : t;  // the row's slot in the partials; < 0: not listed, nothing computed
+  if (r < 0) {
+    if (lse_out) lse_out[t] = 0.0f;
+    logp_out[t] = 0.0f;
+    if (argmax_out) argmax_out[t] = -1;
+    return;
+  }
   float M = -INFINITY;
-  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, partials[static_cast<size_t>(sp) * part_stride + t].x);
+  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, partials[static_cast<size_t>(sp) * part_stride + r].x);
   float S = 0.0f;
   float bv = -INFINITY;
   int32_t bi = 0;
   for (int sp = 0; sp < n_split; ++sp) {
-    const size_t i = static_cast<size_t>(sp) * part_stride + t;
+    const size_t i = static_cast<size_t>(sp) * part_stride + r;
     const float2 pr = partials[i];
     S += pr.y * exp2f(pr.x - M);
     if (best_val[i] > bv) {
@@ -975,7 +982,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) score_finalize_kernel(
     valid = false;
   }
   if (lse_out) lse_out[t] = lse;
-  logp_out[t] = valid ? zy[t] - lse : 0.0f;
+  logp_out[t] = valid ? zy[r] - lse : 0.0f;
   if (argmax_out) argmax_out[t] = bi;
 }
 

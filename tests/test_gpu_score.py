@@ -99,3 +99,35 @@ def test_score_full_size_sampled_rows(cuda_device):
     assert np.max(np.abs(lse.cpu().numpy()[rows] - ref["lse"])) <= TOL_TOKEN
     assert np.max(np.abs(logp.cpu().numpy()[rows] - ref["logp"])) <= TOL_TOKEN
     _check_argmax(argmax.cpu().numpy()[rows], H64, W64)
+
+
+@pytest.mark.parametrize("case", ["rl_T768_H192_V3001", "zipf_T1000_H256_V5000"])
+def test_score_valid_matches_score_on_valid_rows(case, cuda_device):
+    """flce_score_valid skips rows with an ignored target: on every other row lse, logp
+    and the greedy token are bit-identical to flce_score's; skipped rows read 0, 0, -1."""
+    wl, T, Hd, V = CASES[case]
+    inp = generate(wl, T=T, Hd=Hd, V=V, n_seq=8 if wl == "rlpg" else None)
+    if wl != "rlpg":
+        inp.targets[np.random.default_rng(2).random(T) < 0.3] = inp.ignore_index
+    H, W, y, _ = to_device(inp, cuda_device)
+    logp, lse, amax, _ = flce.flce_score(H, W, y, inp.ignore_index)
+    logp_v, lse_v, amax_v, ws = flce.flce_score_valid(H, W, y, inp.ignore_index)
+    assert flce.flce_read_device_status(ws) == 0
+    valid = torch.from_numpy(inp.targets != inp.ignore_index).to(cuda_device)
+    assert 0 < int(valid.sum().item()) < T
+    assert torch.equal(lse[valid], lse_v[valid]) and torch.equal(logp[valid], logp_v[valid])
+    assert torch.equal(amax[valid], amax_v[valid])
+    assert bool((lse_v[~valid] == 0).all().item()) and bool((logp_v[~valid] == 0).all().item())
+    assert bool((amax_v[~valid] == -1).all().item())
+
+
+def test_score_valid_full_size_policy_gradient(cuda_device):
+    """32,768 x 2048 x 124,160 with 30 % of every sequence masked."""
+    inp = generate("rlpg")
+    H, W, y, _ = to_device(inp, cuda_device)
+    logp, lse, amax, _ = flce.flce_score(H, W, y, inp.ignore_index)
+    logp_v, lse_v, amax_v, ws = flce.flce_score_valid(H, W, y, inp.ignore_index)
+    assert flce.flce_read_device_status(ws) == 0
+    valid = torch.from_numpy(inp.targets != inp.ignore_index).to(cuda_device)
+    assert torch.equal(lse[valid], lse_v[valid]) and torch.equal(logp[valid], logp_v[valid])
+    assert torch.equal(amax[valid], amax_v[valid])
