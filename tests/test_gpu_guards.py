@@ -81,6 +81,10 @@ def test_no_write_outside_any_buffer(shape, cuda_device):
     amax = Guarded((T,), torch.int64, dev)
     assert lib.flce_score(P(H.data_ptr()), P(W.data_ptr()), P(y.data_ptr()), T, Hd, V, IGNORE_INDEX, _p(logp),
                           _p(lse), _p(amax), _p(sws), sws.nbytes, s) == 0
+    svws = Guarded((lib.flce_score_valid_workspace_size(T, Hd, V),), torch.uint8, dev)
+    samax = Guarded((T,), torch.int64, dev)
+    assert lib.flce_score_valid(P(H.data_ptr()), P(W.data_ptr()), P(y.data_ptr()), T, Hd, V, IGNORE_INDEX,
+                                _p(vlogp), _p(vlse), _p(samax), _p(svws), svws.nbytes, s) == 0
     cut = max(1, V // 3)
     Wa = W[:cut].contiguous()
     slse = Guarded((T,), torch.float32, dev)
@@ -96,6 +100,7 @@ def test_no_write_outside_any_buffer(shape, cuda_device):
                     ("fwd workspace", fws), ("dH", dH), ("dW", dW), ("bwd workspace", bws),
                     ("score workspace", sws), ("argmax", amax), ("shard_lse", slse), ("shard_zy", szy),
                     ("dH partial", dHp), ("dW shard", dWs), ("valid-forward workspace", vws),
-                    ("valid-forward lse", vlse), ("valid-forward logp", vlogp)]:
+                    ("valid-forward lse", vlse), ("valid-forward logp", vlogp),
+                    ("valid-score workspace", svws), ("valid-score argmax", samax)]:
         assert g.intact(), name
     assert flce.flce_read_device_status(fws.t) == 0 and flce.flce_read_device_status(bws.t) == 0
