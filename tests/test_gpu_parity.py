@@ -365,3 +365,28 @@ def test_gradient_through_logp(cuda_device):
     lp = flce.linear_log_probs(H, W, y)
     ref = oracle.forward(inp.H64(), inp.W64(), inp.targets, inp.ignore_index, "none")
     assert np.max(np.abs(lp.detach().cpu().numpy() - ref.logp)) <= TOL_TOKEN
+
+
+def test_paired_torch_baseline(cuda_device):
+    """The pages' paired-baseline check: swap the primitive, keep the inputs.  The same
+    bf16 inputs through PyTorch's own materialised fp32 logits, cross_entropy and
+    autograd on the GPU give the same loss, per-token logp and gradients within the
+    tolerances (the oracle is the reference everywhere else)."""
+    import torch.nn.functional as F
+
+    inp = generate("medium", T=4096, Hd=1024, V=32000)
+    H, W, y, _ = to_device(inp, cuda_device)
+    Hf = H.float().requires_grad_(True)
+    Wf = W.float().requires_grad_(True)
+    z = Hf @ Wf.T
+    ref_loss = F.cross_entropy(z, y, ignore_index=inp.ignore_index, reduction="mean")
+    ref_loss.backward()
+    ref_logp = torch.where(y == inp.ignore_index, torch.zeros_like(z[:, 0]),
+                           -F.cross_entropy(z.detach(), y.clamp(min=0), reduction="none"))
+    loss, logp = flce.LinearCrossEntropy.apply(H.clone().requires_grad_(True), W, y, inp.ignore_index, "mean")
+    assert abs(float(loss.item()) - float(ref_loss.item())) <= TOL_TOKEN
+    assert float((logp - ref_logp).abs().max().item()) <= TOL_TOKEN
+    dH, dW, _ = flce.flce_backward(torch.ones(1, device=cuda_device), H, W, y,
+                                   flce.flce_forward(H, W, y, inp.ignore_index)[1], inp.ignore_index, "mean")
+    assert rel_fro(dH.float().cpu().numpy(), Hf.grad.double().cpu().numpy()) <= TOL_GRAD
+    assert rel_fro(dW.cpu().numpy(), Wf.grad.double().cpu().numpy()) <= TOL_GRAD
