@@ -60,8 +60,18 @@ def test_random_shape(case, cuda_device):
         assert rel_fro(out["dW"].cpu().numpy(), dW_ref) <= TOL_GRAD
     assert np.all(out["dH"].float().cpu().numpy()[~valid] == 0.0)
 
-    # scoring path on the same inputs
+    # the masked-row forward and scoring give the same numbers on the valid rows
     H, W, y, _ = to_device(inp, cuda_device)
+    vmask = torch.from_numpy(valid).to(cuda_device)
+    fv = flce.flce_forward_valid(H, W, y, IGNORE_INDEX, red)
+    assert flce.flce_read_device_status(fv[4]) == 0
+    assert torch.equal(fv[0], out["loss"]) and torch.equal(fv[2], out["logp"])
+    assert torch.equal(fv[1][vmask], out["lse"][vmask]) and bool((fv[1][~vmask] == 0).all().item())
+    sv = flce.flce_score_valid(H, W, y, IGNORE_INDEX)
+    s_full = flce.flce_score(H, W, y, IGNORE_INDEX)
+    assert torch.equal(sv[0], s_full[0]) and torch.equal(sv[2][vmask], s_full[2][vmask])
+
+    # scoring path on the same inputs
     logp, lse, argmax, _ = flce.flce_score(H, W, y, IGNORE_INDEX)
     assert np.max(np.abs(logp.cpu().numpy() - ref.logp)) <= TOL_TOKEN
     idx, gap = oracle.argmax_rows(H64, W64)
