@@ -113,8 +113,9 @@ FLCE_API size_t flce_backward_workspace_size_for_chunk(int64_t T, int64_t Hd, in
  * 0 if the workspace is too small. */
 FLCE_API int64_t flce_backward_chunk_tokens(int64_t T, int64_t Hd, int64_t V, size_t workspace_bytes);
 
-/* Forward.  Source: section 3 of the first page (logits H W^T reduced row-wise
- * through the running-max / log-sum-exp recurrence; loss per token).
+/* Forward.  Source: "Long-Sequence MoE RL Training: From First Principles to
+ * MI300X", section 3 (logits H W^T reduced row-wise through the running-max /
+ * log-sum-exp recurrence; loss per token).
  *   H        [T, Hd] bf16              hidden states
  *   W        [V, Hd] bf16              LM-head weight
  *   targets  [T] int64                 class per token, or ignore_index
@@ -147,8 +148,9 @@ FLCE_API flce_status flce_forward_valid(const void* H, const void* W, const int6
                                         float* logp, int64_t* n_valid, void* workspace, size_t workspace_bytes,
                                         void* stream);
 
-/* Backward.  Source: section 3 of the first page (recompute the logit tile,
- * form dZ = softmax - onehot for it, contract it into dH and dW at once).
+/* Backward.  Source: the same page and section (each logit tile is formed
+ * again, turned into dZ = softmax - onehot and contracted into dH and dW
+ * straight away).
  *   dloss    [1] fp32 (MEAN, SUM) or [T] fp32 (NONE): gradient of the loss output
  *   H, W, targets, T, Hd, V, ignore_index, reduction: as passed to flce_forward
  *   lse      [T] fp32                  the lse output of flce_forward (or flce_forward_valid)

@@ -156,7 +156,8 @@ def pin_shift_invariance_and_overflow():
     """W -> W + 1 b^T adds h_t.b to every logit of row t: loss, logp, dH and dW are
     unchanged (dZ rows sum to 0) and lse moves by h_t.b.  With h_t.b near 800 an
     un-shifted exp overflows even fp64, so this also pins the running-max correction
-    that section 8 of the first page calls load-bearing."""
+    that section 8 of "Long-Sequence MoE RL Training: From First Principles to
+    MI300X" calls load-bearing."""
     H, W, y = _rand_case(8, T=6, Hd=8, V=33, n_ignore=1)
     b = H.mean(axis=0)
     shift = H @ b
