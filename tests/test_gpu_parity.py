@@ -176,14 +176,24 @@ def test_binding_rejects_buffers_the_library_cannot_use(cuda_device):
     torch.cuda.synchronize()
 
 
-def test_autograd_wrapper(cuda_device):
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_autograd_wrapper(reduction, cuda_device):
+    """linear_cross_entropy through autograd, with a non-trivial upstream gradient for
+    each reduction (a scalar for mean / sum, per-token weights for none)."""
     inp = generate("medium", T=300, Hd=128, V=2000)
     H, W, y, _ = to_device(inp, cuda_device)
     Hr = H.clone().requires_grad_(True)
     Wr = W.clone().requires_grad_(True)
-    loss = flce.linear_cross_entropy(Hr, Wr, y)
-    loss.backward()
-    dH_ref, dW_ref = oracle.backward(1.0, inp.H64(), inp.W64(), inp.targets, -100, "mean")
+    loss = flce.linear_cross_entropy(Hr, Wr, y, reduction=reduction)
+    rng = np.random.default_rng(4)
+    up = (rng.standard_normal(300) if reduction == "none" else np.array([0.7])).astype(np.float32)
+    loss.backward(torch.tensor(up if reduction == "none" else up[0], dtype=torch.float32, device=cuda_device))
+    ref = oracle.forward(inp.H64(), inp.W64(), inp.targets, -100, reduction)
+    if reduction == "none":
+        assert np.max(np.abs(loss.detach().cpu().numpy() - ref.loss_tok)) <= TOL_TOKEN
+    else:
+        assert abs(float(loss.item()) - float(ref.loss)) <= TOL_TOKEN * (1 if reduction == "mean" else ref.n_valid)
+    dH_ref, dW_ref = oracle.backward(up, inp.H64(), inp.W64(), inp.targets, -100, reduction)
     assert rel_fro(Hr.grad.float().cpu().numpy(), dH_ref) <= TOL_GRAD
     assert rel_fro(Wr.grad.float().cpu().numpy(), dW_ref) <= TOL_GRAD
 
