@@ -18,6 +18,7 @@ from .flce_oracle import (  # noqa: F401
     naive_logits_bytes,
     sampled_rows,
     shard_partials,
+    token_outputs_given_lse,
     upstream_grad,
     valid_mask,
 )

@@ -208,6 +208,30 @@ def dW_rows(H: np.ndarray, W_rows: np.ndarray, targets: np.ndarray, g: np.ndarra
     return out
 
 
+def token_outputs_given_lse(H: np.ndarray, W: np.ndarray, targets: np.ndarray, lse: np.ndarray,
+                            ignore_index: int = -100, row_block: int = 8192):
+    """Per-token loss_t = lse_t - z_{t, y_t} and logp_t = -loss_t (0 on ignored rows) on every
+    row, given the oracle's own row normaliser ``lse`` [T] (from :func:`forward`).
+
+    Only the target logit z_{t, y_t} = h_t . w_{y_t} of each row is formed (T dot products
+    of length Hd instead of T x V), so a stored lse turns into the per-token outputs of a
+    large batch cheaply.  Same definitions as :func:`forward` (section 3 of the page).
+    """
+    H = np.asarray(H)
+    W = np.asarray(W)
+    targets = np.asarray(targets, dtype=np.int64)
+    valid = valid_mask(targets, W.shape[0], ignore_index)
+    zy = np.zeros(H.shape[0])
+    for r0 in range(0, H.shape[0], row_block):
+        r1 = min(H.shape[0], r0 + row_block)
+        v = valid[r0:r1]
+        Hb = np.asarray(H[r0:r1][v], dtype=np.float64)
+        Wb = np.asarray(W[targets[r0:r1][v]], dtype=np.float64)
+        zy[r0:r1][v] = np.einsum("ij,ij->i", Hb, Wb)
+    loss_tok = np.where(valid, np.asarray(lse, dtype=np.float64) - zy, 0.0)
+    return {"loss_tok": loss_tok, "logp": -loss_tok}
+
+
 def shard_partials(H: np.ndarray, W_shard: np.ndarray, targets: np.ndarray, vocab_offset: int,
                    ignore_index: int = -100, row_block: int = 256):
     """Per-row partials of one vocab shard: the log-sum-exp over the shard's logit
@@ -264,6 +288,6 @@ def naive_logits_bytes(T: int, V: int, bytes_per_elem: int, copies: int = 1) -> 
 
 __all__ = [
     "ForwardResult", "argmax_rows", "backward", "dW_rows", "forward", "logits", "naive_logits_bytes",
-    "sampled_rows", "shard_partials", "upstream_grad", "valid_mask", "REDUCTIONS",
+    "sampled_rows", "shard_partials", "token_outputs_given_lse", "upstream_grad", "valid_mask", "REDUCTIONS",
 ]
 

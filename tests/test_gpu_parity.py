@@ -5,17 +5,21 @@ Element-by-element on shapes the oracle finishes in seconds that span several
 on the five full-size workloads.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import lm_head_linear_gb300 as flce
 import oracle
-from workloads import generate, workload
+from workloads import generate, inputs_digest, workload
 
 from gpu_helpers import TOL_GRAD, TOL_TOKEN, check_token_outputs, rel_fro, run, to_device
 
 pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 # name -> (workload recipe, T, Hd, V): every case spans several tiles and has ragged edges.
 FULL_CASES = {
@@ -207,7 +211,10 @@ FULL_SIZE = ["tiny", "medium", "lmhead", "long", "rlpg"]
 def test_full_size_workload(name, cuda_device):
     """Full-size run in the bench's launch configuration: sampled token rows against the
     oracle (lse, logp, loss, dH), and for dW the properties that hold at any size:
-    sum_v dW_v = 0 up to the bf16 rounding of dZ, and <dW, W> = <dH, H>."""
+    sum_v dW_v = 0 up to the bf16 rounding of dZ, and <dW, W> = <dH, H>.  On the three
+    largest workloads also every token's lse, logp and loss and sampled vocab rows of dW
+    (tile and box edges, the most frequent targets, random rows) against the oracle,
+    through the oracle's stored lse of the workload (tests/golden/)."""
     wl = workload(name)
     inp = generate(wl)
     torch.cuda.reset_peak_memory_stats(cuda_device)
@@ -258,6 +265,70 @@ def test_full_size_workload(name, cuda_device):
     rhs = float((dH.double() * H_dev.double()).sum().item())
     assert abs(lhs - rhs) <= TOL_GRAD * max(abs(lhs), abs(rhs)) + 1e-6, (lhs, rhs)
     assert float(dW.abs().max().item()) > 0.0
+    del H_dev, W_dev, dH
+
+    gold = load_lse_golden(wl)
+    if gold is not None:
+        _check_against_stored_lse(inp, out, gold, g)
+
+
+def load_lse_golden(wl):
+    """The oracle's per-token lse of a full-size workload, stored by
+    tests/golden/make_lse_golden.py (None for workloads that have none)."""
+    path = os.path.join(GOLDEN, f"lse_{wl.name}.npz")
+    if not os.path.exists(path):
+        return None
+    d = np.load(path)
+    return {"lse": d["lse"].astype(np.float64), "seed": int(d["seed"]), "T": int(d["T"]), "Hd": int(d["Hd"]),
+            "V": int(d["V"]), "inputs_sha256": str(d["inputs_sha256"])}
+
+
+def dW_sample_rows(inp, n_random=16, seed=11):
+    """Vocab rows for the sampled dW check: both ends, rows on either side of the 64-row
+    TMA box, 128-row CTA block and 256-row pair-tile edges (first tiles and last full
+    tile), random rows, and the most frequent targets."""
+    V = inp.V
+    edges = [0, 1, 63, 64, 127, 128, 255, 256, 257, 511, 512]
+    last_tile = (V // 256) * 256
+    edges += [last_tile - 257, last_tile - 256, last_tile - 1, last_tile, V - 65, V - 64, V - 2, V - 1]
+    valid = inp.targets != inp.ignore_index
+    counts = np.bincount(inp.targets[valid], minlength=V)
+    frequent = np.argsort(-counts, kind="stable")[:4]
+    rnd = np.random.default_rng(seed).choice(V, n_random, replace=False)
+    rows = np.concatenate([edges, frequent, rnd])
+    return np.unique(rows[(rows >= 0) & (rows < V)])
+
+
+def _check_against_stored_lse(inp, out, gold, g):
+    """Every token's lse / logp and sampled vocab rows of dW against the oracle, through
+    the oracle's stored lse of this workload (one fp64 pass over T x V, made once)."""
+    assert (gold["seed"], gold["T"], gold["Hd"], gold["V"]) == (0, inp.T, inp.Hd, inp.V)
+    assert inputs_digest(inp) == gold["inputs_sha256"], "inputs differ from those the stored lse was made from"
+    lse_ref = gold["lse"]
+    valid = inp.targets != inp.ignore_index
+    # per-token outputs on every row (the stored lse is the oracle's; z_y from the inputs)
+    lse = out["lse"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse - lse_ref)) <= TOL_TOKEN, np.max(np.abs(lse - lse_ref))
+    H64 = inp.H64()
+    tok = oracle.token_outputs_given_lse(H64, inp.W64(), inp.targets, lse_ref, inp.ignore_index)
+    logp_ref = tok["logp"]
+    logp = out["logp"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(logp - logp_ref)) <= TOL_TOKEN, np.max(np.abs(logp - logp_ref))
+    assert np.all(logp[~valid] == 0.0)
+    if inp.reduction == "none":
+        loss = out["loss"].cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(loss + logp_ref)) <= TOL_TOKEN
+    else:
+        loss_ref = float(np.sum(-logp_ref)) / (int(valid.sum()) if inp.reduction == "mean" else 1)
+        tol = TOL_TOKEN * (1 if inp.reduction == "mean" else int(valid.sum()))
+        assert abs(float(out["loss"].item()) - loss_ref) <= tol, (float(out["loss"].item()), loss_ref)
+    # sampled vocab rows of dW
+    vr = dW_sample_rows(inp)
+    dW_ref = oracle.dW_rows(H64, inp.W64(vr), inp.targets, g, lse_ref, vr)
+    dW_rows = out["dW"][torch.from_numpy(vr).to(out["dW"].device)].cpu().numpy().astype(np.float64)
+    per_row = [rel_fro(dW_rows[i], dW_ref[i]) for i in range(len(vr))]
+    assert rel_fro(dW_rows, dW_ref) <= TOL_GRAD, (rel_fro(dW_rows, dW_ref), max(per_row))
+    assert max(per_row) <= TOL_GRAD, dict(zip(vr.tolist(), per_row))
 
 
 def test_dz_block_beyond_2_31_elements(cuda_device):

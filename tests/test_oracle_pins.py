@@ -281,6 +281,13 @@ def pin_sampled_paths():
     vr = np.array([0, 5, 39, 17])
     dWr = fo.dW_rows(H, W[vr], y, g, f.lse, vr, token_block=3)
     assert np.allclose(dWr, dW[vr], atol=1e-14)
+    t = fo.token_outputs_given_lse(H, W, y, f.lse, IGN, row_block=4)
+    assert np.allclose(t["loss_tok"], f.loss_tok, atol=1e-13) and np.allclose(t["logp"], f.logp, atol=1e-13)
+    assert np.all(t["logp"][y == IGN] == 0.0)
+    # brute force on one valid row: z_y by a Python loop
+    r = int(np.nonzero(y != IGN)[0][0])
+    zy = sum(H[r][k] * W[y[r]][k] for k in range(8))
+    assert abs(t["logp"][r] - (zy - f.lse[r])) < 1e-12
 
 
 def pin_vocab_shards():

@@ -15,5 +15,6 @@ from .synth import (  # noqa: F401
     bf16_bits_to_f32,
     bf16_bits_to_f64,
     generate,
+    inputs_digest,
     workload,
 )

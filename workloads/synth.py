@@ -134,6 +134,16 @@ class Inputs:
         return bf16_bits_to_f64(self.W_bits if rows is None else self.W_bits[rows])
 
 
+def inputs_digest(inp: "Inputs") -> str:
+    """sha256 over one drawn batch (bf16 bits of H and W, targets, upstream gradient) in a
+    fixed order and byte layout: identifies the inputs a stored expected value was made from."""
+    import hashlib
+    h = hashlib.sha256()
+    for a in (inp.H_bits, inp.W_bits, inp.targets.astype("<i8"), inp.dloss.astype("<f4")):
+        h.update(np.ascontiguousarray(a).tobytes())
+    return h.hexdigest()
+
+
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bits.
 
