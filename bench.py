@@ -62,18 +62,29 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+def traffic_from_profiles(kernel, T, Hd, V, chunk=None):
+    """DRAM bytes per launch of `kernel` at T x Hd x V, from the committed ncu summary of
+    a smaller case (profiles/traffic.json), if it was taken on the current kernel sources
+    (else None).  The backward kernels work on one token chunk per launch; at the same
+    chunk and Hd their tiles, and their DRAM bytes, grow in proportion to V, so the small
+    case's median is scaled by V / V_case.  The forward's traffic does not grow in
+    proportion to its tiles (it depends on which operand blocks stay in L2), so it is not
+    scaled and is reported only for the captured shape itself."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         data = json.load(fh)
-    rec = data.get(kernel)
-    if not rec or rec.get("source_sha") != kernel_source_sha():
+    if data.get("source_sha") != kernel_source_sha():
         return None
-    return rec.get("dram_bytes_per_launch")
+    case = data.get("case", {})
+    rec = data.get("kernels", {}).get(kernel)
+    if not rec or case.get("Hd") != Hd:
+        return None
+    per_launch = float(rec["per_launch_median"])
+    if rec.get("scale") == "V":
+        return per_launch * V / float(case["V"]) if chunk == case.get("chunk") else None
+    return per_launch if (case.get("T"), case.get("V")) == (T, V) else None
 
 
 class ClockSampler:
@@ -162,6 +173,43 @@ def dist_setup():
     return world, rank, local
 
 
+def free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(nprocs, argv, env=None):
+    """Runs ``argv`` (a script and its arguments) as ``nprocs`` ranks of one node through
+    torch.distributed.run, with the rendezvous on 127.0.0.1; every rank gets RANK,
+    LOCAL_RANK and WORLD_SIZE.  Returns the launcher's exit code (non-zero when a rank
+    failed)."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={int(nprocs)}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", *argv]
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.call(cmd, env=e)
+
+
+def spawn_self(args):
+    """``--gpus N`` (N > 1) outside a launcher: start N ranks of this script, one per GPU.
+    The replicas exchange nothing on the data path; NCCL carries the barriers and the
+    max-over-ranks reduction of the timed region, and its communicator lines are printed
+    (NCCL_DEBUG=INFO for the INIT subsystem unless the caller set NCCL_DEBUG)."""
+    if args.impl == "ours":
+        import torch
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            print(f"bench.py: --gpus {args.gpus} needs {args.gpus} visible GPUs, this process sees {have}",
+                  file=sys.stderr, flush=True)
+            return 2
+    env = {}
+    if "NCCL_DEBUG" not in os.environ:
+        env = {"NCCL_DEBUG": "INFO", "NCCL_DEBUG_SUBSYS": "INIT"}
+    return launch_ranks(args.gpus, [os.path.abspath(__file__), *sys.argv[1:]], env)
+
+
 def time_oracle(inp, budget_s=12.0, slice_tokens=128, W64=None):
     """Tokens/s of the fp64 oracle (as it stands) on slices of the workload's tokens:
     forward + backward for each slice with the full vocabulary."""
@@ -205,9 +253,13 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = sum(r["value"] for r in per) / len(per)
     tokens = value * el
+    # Each timed step is a bounded sample (a few seconds of token slices), so ms_per_step is
+    # the measured wall time of one such step; the time the oracle would take for the whole
+    # batch of T tokens at the same rate is reported beside it.
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * inp.T / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps,
+        "ms_per_full_batch_extrapolated": 1000.0 * inp.T / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name, "T": inp.T, "Hd": inp.Hd, "V": inp.V,
                                         "reduction": wl.reduction},
@@ -450,8 +502,12 @@ def run_ours(args):
 
     world, rank, local = dist_setup()
     if world > 1:
+        if torch.cuda.device_count() <= local:
+            print(f"bench.py: rank {rank} has local rank {local} but sees {torch.cuda.device_count()} GPUs",
+                  file=sys.stderr, flush=True)
+            return 2
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     wl = workload(args.workload)
@@ -614,8 +670,10 @@ def run_ours(args):
     dom_name, dom = max(kstats.items(), key=lambda kv: kv[1]["total_ms"])
     avg_ms = dom["total_ms"] / dom["launches"]
     ach = (dom["flops"] / dom["launches"]) / (avg_ms / 1000.0) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    traffic = traffic_from_profiles(dom_name) if args.path == "loss" else None
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = (traffic_from_profiles(dom_name, T, Hd, V, path.config().get("backward_chunk_tokens"))
+               if args.path == "loss" else None)
     kernels = {k: {"launches": v["launches"], "avg_ms": v["total_ms"] / v["launches"],
                    "share": v["total_ms"] / sum(x["total_ms"] for x in kstats.values()),
                    "tflops": (v["flops"] / (v["total_ms"] / 1000.0) / 1e12) if v["flops"] else None}
@@ -637,11 +695,12 @@ def run_ours(args):
         "tflops": tflops,
         "tflops_executed": tflops_exec,
         "frac_of_bf16_peak": {"burst": tflops_exec / float(peaks.get("bf16_tflops", 1)),
-                              "sustained": tflops_exec / peak, "source": peak_src,
+                              "sustained": tflops_exec / peak_sus, "source": peak_src,
                               "flops": "executed: 2*T*Hd*V forward + 6*Hd*V per row the backward contracts"},
         "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                      "frac": ach / peak, "traffic": traffic,
-                     "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                     "peak_kind": f"bf16_tflops, burst ({peak_src})",
+                     "peak_sustained": peak_sus, "frac_sustained": ach / peak_sus,
                      "algorithmic_flops_per_launch": dom["flops"] / dom["launches"]},
         "kernels": kernels,
         "gpu_launches": int(gpu_launches),
@@ -683,6 +742,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and world == 1:
+        return spawn_self(args)
+    if world > 1 and args.gpus != world:
+        print(f"bench.py: --gpus {args.gpus} but the launcher started {world} ranks", file=sys.stderr, flush=True)
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
