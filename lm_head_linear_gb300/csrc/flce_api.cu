@@ -391,26 +391,62 @@ flce_status check_common(const void* H, const void* W, const int64_t* targets, i
 // ------------------------------------------------------------------ built-in scratch
 // Scratch of flce_forward_noalloc(): a device array of fixed size in this
 // library's module.  Host code must not use the symbol as a pointer; the
-// device address comes from cudaGetSymbolAddress, once per device.
+// device address comes from cudaGetSymbolAddress with the device current.
+// The address belongs to the module as loaded into one context, so it is
+// remembered per (device, current context): a context created after
+// cudaDeviceReset, or another context made current on the same device, loads
+// the module again and gets its address looked up again.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};
+struct ScratchSlot {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
+ScratchSlot g_scratch_slot[64];
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
 
 flce_status static_scratch_address(void** out) {
   int dev = 0;
   CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return fail(FLCE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || !p)
+  if (!g_ctx_get_current) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    if (!g_ctx_get_current) return fail(FLCE_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+  }
+  auto lookup = [&](void** p) -> flce_status {
+    const cudaError_t e = cudaGetSymbolAddress(p, g_static_scratch);
+    if (e != cudaSuccess || !*p)
       return fail(FLCE_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed on device %d: %s", dev,
                   cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+    return FLCE_OK;
+  };
+  ScratchSlot& slot = g_scratch_slot[dev];
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  if (!ctx) {
+    // No context yet on this thread: the runtime call below makes the device's
+    // primary context current, and the address is remembered for that context.
+    void* p = nullptr;
+    flce_status st = lookup(&p);
+    if (st != FLCE_OK) return st;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx)
+      return fail(FLCE_ERR_CUDA, "no current CUDA context on device %d", dev);
+    slot.ctx = ctx;
+    slot.addr = p;
+  } else if (slot.ctx != ctx || !slot.addr) {
+    void* p = nullptr;
+    flce_status st = lookup(&p);
+    if (st != FLCE_OK) return st;
+    slot.ctx = ctx;
+    slot.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return FLCE_OK;
 }
 
@@ -1130,6 +1166,8 @@ flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* ta
                                  int64_t V, int64_t ignore_index, int32_t reduction, float* loss, float* lse,
                                  float* logp, int64_t* n_valid, int32_t* device_status, void* stream) {
   if (T < 0 || V < 1) return fail(FLCE_ERR_INVALID_ARG, "T = %lld or V = %lld out of range", (long long)T, (long long)V);
+  flce_status st = check_common(H, W, targets, T, Hd, V, ignore_index, reduction);
+  if (st != FLCE_OK) return st;
   const size_t need = flce_forward_workspace_size(T, Hd, V);
   if (need > kStaticScratchBytes)
     return fail(FLCE_ERR_WORKSPACE,
@@ -1137,7 +1175,7 @@ flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* ta
                 (long long)T, need, kStaticScratchBytes);
   if (misaligned(device_status)) return fail(FLCE_ERR_ALIGNMENT, "device_status must be 4-byte aligned");
   void* scratch = nullptr;
-  flce_status st = static_scratch_address(&scratch);
+  st = static_scratch_address(&scratch);
   if (st != FLCE_OK) return st;
   st = flce_forward(H, W, targets, T, Hd, V, ignore_index, reduction, loss, lse, logp, n_valid, scratch,
                     kStaticScratchBytes, stream);

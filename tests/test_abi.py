@@ -121,6 +121,24 @@ def test_misaligned_typed_arrays_are_rejected_on_the_host(lib):
     assert st == 3
 
 
+def test_noalloc_forward_size_limit_on_the_host(lib):
+    """flce_forward_noalloc's built-in scratch holds 32 MiB: the documented maximum of
+    253,952 tokens fits it at any Hd and V, one 128-token step more does not.  At the
+    maximum the size check passes and the next argument check (a NULL H) answers; above
+    it the call is refused as a workspace error.  Nothing is launched either way."""
+    for Hd in (64, 2048, 4096, 16384):
+        for V in (1, 4096, 124160, 300001):
+            assert lib.flce_forward_workspace_size(253952, Hd, V) <= 32 << 20
+            assert lib.flce_forward_workspace_size(253952 + 128, Hd, V) > 32 << 20
+    P = ctypes.c_void_p
+    st = lib.flce_forward_noalloc(None, P(16), P(16), 253952, 64, 300, -100, 1, P(16), P(16), P(16), None, None,
+                                  None)
+    assert st == 1 and b"NULL" in lib.flce_last_error()
+    st = lib.flce_forward_noalloc(P(16), P(16), P(16), 253952 + 128, 64, 300, -100, 1, P(16), P(16), P(16), None,
+                                  None, None)
+    assert st == 4 and b"scratch" in lib.flce_last_error()
+
+
 def test_backward_workspace_for_a_chunk_round_trips(lib):
     """flce_backward_workspace_size_for_chunk(c) is the smallest workspace that runs
     chunks of c rows (capped at T rounded up to 128), on ragged and large shapes."""

@@ -4,8 +4,8 @@ Some callers cannot allocate device memory where they need the loss (their
 framework's allocator owns the device memory, or they run inside an engine
 hook that may not allocate).  flce_forward_noalloc serves them with a scratch
 array built into the library.  This test checks that it gives the same loss,
-lse, logp and n_valid as flce_forward with a caller-provided workspace, within
-the parity tolerances, on two calls in a row that reuse the shared scratch
+lse, logp and n_valid as flce_forward with a caller-provided workspace (within
+the parity tolerances, and in fact bit for bit), on two calls in a row that reuse the shared scratch
 with different shapes and reductions, and that it rejects a T the scratch
 cannot hold.  The file name makes pytest collect it last.
 """
@@ -55,6 +55,8 @@ def test_noalloc_forward_matches_forward_on_two_calls(cuda_device):
         for got, want in ((loss, ref_loss), (lse, ref_lse), (logp, ref_logp)):
             assert torch.isfinite(got).all()
             assert float((got - want).abs().max().item()) <= TOL_TOKEN
+            # the same kernels on the same inputs, in the same order: bit for bit
+            assert torch.equal(got, want)
 
 
 def test_noalloc_forward_reports_device_status_and_rejects_large_T(cuda_device):
