@@ -161,6 +161,25 @@ flce_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, ui
   return FLCE_OK;
 }
 
+// 3-D map over the dZ block stored as 64-column panels: {64 columns, rows,
+// panels}, rows of 128 bytes, panels `rows` x 128 bytes apart; box {64,
+// box_rows, 1}; 128-byte swizzle.  Out-of-range panels read as zero, stores
+// there are clipped.
+flce_status make_panel_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t panels, uint32_t box_rows) {
+  cuuint64_t dims[3] = {64, rows, panels};
+  cuuint64_t strides[2] = {128, 128 * rows};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for panels {64, %llu, %llu} box rows %u",
+                static_cast<int>(r), static_cast<unsigned long long>(rows), static_cast<unsigned long long>(panels),
+                box_rows);
+  return FLCE_OK;
+}
+
 // ------------------------------------------------------------------ profiling
 struct LaunchRecord {
   int kind;
@@ -317,7 +336,7 @@ constexpr size_t kRowCountOff = 16;  // backward header: length of the row list 
 
 // Header (status word, row count) | tile counters (one per possible chunk) |
 // g [T] | row list [T] | H rows of the chunk [chunk, Hd] | dH rows of the chunk
-// [chunk, Hd] | dZ chunk [chunk, V_pad].
+// [chunk, Hd] | dZ chunk: V_pad / 64 panels of [chunk, 64] (DzPanels).
 BwdLayout bwd_layout(int64_t T, int64_t Hd, int64_t V, int64_t chunk) {
   BwdLayout L{};
   L.chunk = chunk;
@@ -617,12 +636,11 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
   if ((st = make_map(&tm_Hc_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hc, Hd, chunk, Hd * 2, 64, 64)) != FLCE_OK) return st;
   if ((st = make_map(&tm_dHc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dHc, Hd, chunk, Hd * 2, 64, 32)) != FLCE_OK) return st;
   if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_dz_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, chunk, L.v_pad * 2, 64, 32)) != FLCE_OK)
-    return st;
-  if ((st = make_map(&tm_dz_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, chunk, L.v_pad * 2, BK, BM)) != FLCE_OK)
-    return st;
-  if ((st = make_map(&tm_dz_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, V, chunk, L.v_pad * 2, 64, 64)) != FLCE_OK)
-    return st;
+  // dZ block: V_pad / 64 panels of [chunk x 64] (the kernels' DzPanels layout)
+  const uint64_t dz_panels = static_cast<uint64_t>(L.v_pad / 64);
+  if ((st = make_panel_map(&tm_dz_store, dz, chunk, dz_panels, 32)) != FLCE_OK) return st;
+  if ((st = make_panel_map(&tm_dz_k, dz, chunk, dz_panels, BM)) != FLCE_OK) return st;
+  if ((st = make_panel_map(&tm_dz_mn, dz, chunk, dz_panels, 64)) != FLCE_OK) return st;
 
   const int64_t n_chunks = cdiv(T, chunk);
   int32_t* counters = reinterpret_cast<int32_t*>(ws + L.cnt_off);

@@ -88,13 +88,19 @@ __host__ __device__ constexpr int smem_bytes_for(int mode) {
 static_assert(smem_bytes_for(MODE_DHW) <= 232448, "shared memory per CTA");
 static_assert(kBarriers * 8 + 8 + kTileRing * 4 <= kSmemTail, "smem tail");
 
+// DzPanels: the backward's [chunk x V] bf16 dZ block is stored as V_pad / 64
+// panels of 64 vocab columns, each panel [chunk rows x 64 columns] row-major
+// (128 bytes per row), panel after panel.  Its three tensor maps are 3-D
+// {64 columns, rows, panels}; every box the kernels move (32 x 64 stored, 128 x 64
+// and 64 x 64 loaded) is then one contiguous run of memory instead of 32..128
+// rows 2 V bytes apart.
 struct GemmParams {
-  // MODE_FWD / MODE_DZ: A = H (K-major), B = W (K-major), tmOut = dZ store.
-  // MODE_DHW dH tiles: A = dZ (K-major), B = W (MN-major), tmOut = dH store.
+  // MODE_FWD / MODE_DZ: A = H (K-major), B = W (K-major), tmOut = dZ store (panels).
+  // MODE_DHW dH tiles: A = dZ (K-major, panels), B = W (MN-major), tmOut = dH store.
   CUtensorMap tmA;
   CUtensorMap tmB;
   CUtensorMap tmOut;
-  // MODE_DHW dW tiles: A = dZ (MN-major), B = H (MN-major), tmOut2 = dW store / reduce.
+  // MODE_DHW dW tiles: A = dZ (MN-major, panels), B = H (MN-major), tmOut2 = dW store / reduce.
   CUtensorMap tmA2;
   CUtensorMap tmB2;
   CUtensorMap tmOut2;
@@ -284,19 +290,23 @@ __device__ __forceinline__ void load_logits_stage(const GemmParams& p, uint32_t 
 }
 
 // dH tile: dZ rows (K-major, K = vocab) and W as MN-major 64-column boxes.
+// The dZ block is stored in 64-column panels (see DzPanels): K block k0 / 64
+// of 128 token rows is one contiguous 16 KB piece of panel k0 / 64.
 __device__ __forceinline__ void load_dh_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst, uint32_t full,
                                               int m_blk, int nb, int k0, uint32_t rank) {
-  ptx::tma_load_2d_pair(a_dst, &p.tmA, k0, m_blk * BM, full);
+  ptx::tma_load_3d_pair(a_dst, &p.tmA, 0, m_blk * BM, k0 / BK, full);
 #pragma unroll
   for (int j = 0; j < BN_HALF / 64; ++j)
     ptx::tma_load_2d_pair(b_dst + j * 8192, &p.tmB, nb * BN + static_cast<int>(rank) * BN_HALF + j * 64, k0, full);
 }
 
 // dW tile: dZ^T (MN-major 64-vocab boxes, K = tokens) and H[chunk] as MN-major boxes.
+// 64 vocab rows x 64 tokens of dZ^T are 64 consecutive 128-byte rows of one panel.
 __device__ __forceinline__ void load_dw_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst, uint32_t full,
                                               int m_blk, int nb, int k0, uint32_t rank) {
 #pragma unroll
-  for (int j = 0; j < BM / 64; ++j) ptx::tma_load_2d_pair(a_dst + j * 8192, &p.tmA2, m_blk * BM + j * 64, k0, full);
+  for (int j = 0; j < BM / 64; ++j)
+    ptx::tma_load_3d_pair(a_dst + j * 8192, &p.tmA2, 0, k0, (m_blk * BM) / 64 + j, full);
 #pragma unroll
   for (int j = 0; j < BN_HALF / 64; ++j)
     ptx::tma_load_2d_pair(b_dst + j * 8192, &p.tmB2, nb * BN + static_cast<int>(rank) * BN_HALF + j * 64,
@@ -406,9 +416,11 @@ __device__ __forceinline__ void stage_row_words(uint32_t buf, int lane, const ui
 }
 
 // Stages one 32-row x 128-byte box in a staging buffer (alternating two per
-// warp) and stores or reduce-adds it with TMA at (x, yrow).
+// warp) and stores or reduce-adds it with TMA at (x, yrow), or, with panel >= 0,
+// stores it at (0, yrow, panel) of a map over 64-column panels.
 __device__ __forceinline__ void store_box(const CUtensorMap* tm, bool reduce, uint32_t staging0,
-                                          uint32_t& box_count, int lane, const uint32_t (&w)[32], int x, int yrow) {
+                                          uint32_t& box_count, int lane, const uint32_t (&w)[32], int x, int yrow,
+                                          int panel = -1) {
   const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
   if (lane == 0) ptx::bulk_wait_read<1>();
   __syncwarp();
@@ -416,7 +428,9 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tm, bool reduce, ui
   ptx::fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (reduce)
+    if (panel >= 0)
+      ptx::tma_store_3d(tm, buf, 0, yrow, panel);
+    else if (reduce)
       ptx::tma_reduce_add_2d(tm, buf, x, yrow);
     else
       ptx::tma_store_2d(tm, buf, x, yrow);
@@ -426,11 +440,13 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tm, bool reduce, ui
 }
 
 // bf16 tile store (dZ or dH): 4 boxes of 64 columns.  With DZ set, each
-// accumulator value z becomes g (2^(z log2e - lse log2e) - [col == y]).
+// accumulator value z becomes g (2^(z log2e - lse log2e) - [col == y]), columns
+// at or past V become 0 (the last panel's tail is read back as K by the dH
+// tiles), and box j goes to panel x0 / 64 + j of the dZ block.
 template <bool DZ>
 __device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tcol, int x0, int yrow,
                                               uint32_t staging0, uint32_t& box_count, int lane, float gt,
-                                              float lse2, int y) {
+                                              float lse2, int y, int V = 0) {
 #pragma unroll 1
   for (int j = 0; j < BN / 64; ++j) {
     uint32_t w[32];
@@ -450,11 +466,16 @@ __device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tc
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gt;
+        if (col0 + 32 > V) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + i >= V) v[i] = 0.0f;
+        }
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) w[h * 16 + i] = ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]);
     }
-    store_box(tm, false, staging0, box_count, lane, w, x0 + j * 64, yrow);
+    store_box(tm, false, staging0, box_count, lane, w, x0 + j * 64, yrow, DZ ? x0 / 64 + j : -1);
   }
 }
 
@@ -613,7 +634,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const Counts&
           }
         } else {
           epi_bf16_tile<true>(&p.tmOut, tcol, nb * BN, un.m_blk * BM + q * 32, staging0, box_count, lane, gt, lse2,
-                              y);
+                              y, p.V);
         }
       }
       release_accumulator(s, acc, lane);
