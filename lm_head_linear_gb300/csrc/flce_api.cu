@@ -706,13 +706,18 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     p.num_n_blocks = static_cast<int32_t>(n_hd_blocks);
     p.num_k_blocks = static_cast<int32_t>(cdiv(V, BK));
     p.num_k_blocks2 = static_cast<int32_t>(cdiv(chunk, BK));
-    p.n_dh_tiles = static_cast<int32_t>(cap_pairs * n_hd_blocks);
+    // dH tiles 256 x 512 when the hidden size splits into 512-column blocks: one
+    // A block (dZ rows) feeds two N = 256 MMAs, so each SM moves 25 % fewer
+    // operand bytes per FLOP than with 256 x 256 tiles.
+    p.dh_wide = (Hd % (2 * BN) == 0) ? 1 : 0;
+    p.n_dh_tiles = static_cast<int32_t>(cap_pairs * (p.dh_wide ? n_hd_blocks / 2 : n_hd_blocks));
     p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
     p.reduce_out = c > 0 ? 1 : 0;
     p.tile_counter = counters + c;
     p.dW_zero = dW;
     p.dW_elems = V * Hd;
-    p.timeout_ns = wait_limit_ns(std::max<int64_t>(V, chunk));  // dH tiles: K = V; dW tiles: K = the chunk
+    // dH tiles: K = V (twice the work per unit of K when wide); dW tiles: K = the chunk
+    p.timeout_ns = wait_limit_ns(std::max<int64_t>(p.dh_wide ? 2 * V : V, chunk));
     {
       const int grid = 2 * static_cast<int>(std::min<int64_t>(dev->pairs[MODE_DHW], p.n_dh_tiles + p.n_dw_tiles));
       KernelScope ks(FLCE_KERNEL_BWD_DH_DW, s, 0.0, 2.0 * V * Hd + (c > 0 ? 8.0 : 4.0) * V * Hd, row_count, c0,

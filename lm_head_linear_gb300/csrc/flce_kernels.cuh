@@ -59,6 +59,15 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN_HALF * BK * 2;       // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
 constexpr uint32_t PAIR_TX_BYTES = 2 * STAGE_BYTES;  // both CTAs' loads of a stage
+// MODE_DHW wide dH tiles (256 tokens x 512 hidden columns per pair): a stage holds
+// the A block and two 128-column halves of B, and the same 192 KB of shared
+// memory is cut into 4 such stages instead of 6.
+constexpr int WIDE_NSTAGE = 4;
+constexpr int WIDE_B_BYTES = 2 * B_BYTES;                  // 32 KB
+constexpr int WIDE_STAGE_BYTES = A_BYTES + WIDE_B_BYTES;   // 48 KB per CTA
+constexpr uint32_t WIDE_PAIR_TX_BYTES = 2 * WIDE_STAGE_BYTES;
+static_assert(WIDE_NSTAGE * WIDE_STAGE_BYTES <= NSTAGE * STAGE_BYTES, "wide stages fit the ring");
+static_assert(WIDE_STAGE_BYTES % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int STAGING_BOX_BYTES = 32 * 128;     // 32 rows x 128 bytes
@@ -118,6 +127,7 @@ struct GemmParams {
   int32_t n_dh_tiles;    // MODE_DHW: dH tiles come first in the tile order ...
   int32_t n_dw_tiles;    // ... then the dW tiles
   int32_t num_k_blocks2; // MODE_DHW: K blocks of a dW tile (tokens of the chunk / 64)
+  int32_t dh_wide;       // MODE_DHW: 1 = dH tiles are 256 x 512 (both TMEM accumulators), 0 = 256 x 256
   int64_t vocab_offset;  // global id of local vocab row 0 (a vocab shard); 0 for the full vocabulary
   int64_t ignore_index;
   const int64_t* targets;
@@ -167,7 +177,7 @@ __device__ __forceinline__ Counts counts_of(const GemmParams& p) {
   c.rows = min(max(*p.rows_dev - p.index0, 0), p.rows);
   c.num_m_pairs = (c.rows + 2 * BM - 1) / (2 * BM);
   c.num_units = c.num_m_pairs * (is_forward(MODE) ? p.n_split : p.num_n_blocks);
-  c.n_dh_tiles = c.num_m_pairs * p.num_n_blocks;
+  c.n_dh_tiles = c.num_m_pairs * (p.dh_wide ? p.num_n_blocks / 2 : p.num_n_blocks);
   c.num_k_blocks2 = (c.rows + BK - 1) / BK;
   return c;
 }
@@ -212,19 +222,24 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const Counts& c
 
 // One MODE_DHW tile: family 0 = dH, family 1 = dW; Hd blocks fastest so that
 // CTAs running side by side share the dZ rows (dH) or dZ columns (dW) in L2.
+// With p.dh_wide, a dH tile covers 512 hidden columns (nb counts 512-column
+// blocks) and uses both TMEM accumulators.
 struct Tile {
   int family;
   int m_blk;
   int nb;
   int num_k;
+  bool wide;
 };
 
 __device__ __forceinline__ Tile decode_dhw(const GemmParams& p, const Counts& c, int t, uint32_t rank) {
   Tile r;
   r.family = t < c.n_dh_tiles ? 0 : 1;
+  r.wide = r.family == 0 && p.dh_wide != 0;
   const int u = r.family ? t - c.n_dh_tiles : t;
-  const int pair = u / p.num_n_blocks;
-  r.nb = u - pair * p.num_n_blocks;
+  const int nbl = r.wide ? p.num_n_blocks / 2 : p.num_n_blocks;
+  const int pair = u / nbl;
+  r.nb = u - pair * nbl;
   r.m_blk = 2 * pair + static_cast<int>(rank);
   r.num_k = r.family ? c.num_k_blocks2 : p.num_k_blocks;
   return r;
@@ -313,48 +328,95 @@ __device__ __forceinline__ void load_dw_stage(const GemmParams& p, uint32_t a_ds
                           p.row0 + k0, full);
 }
 
-// Ring bookkeeping of the producer: which stages hold loads, and their phase.
-struct ProducerState {
-  uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
-  __device__ __forceinline__ void advance() {
-    issued_mask |= 1u << stage;
-    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-    if (++stage == NSTAGE) {
-      stage = 0;
-      phase ^= 1u;
-    }
+// Wide dH tile: the A block as for dH, and B as two halves of 128 hidden
+// columns each (the pair MMA's N = 256 halves of this CTA for hidden columns
+// nb*512 + 128*rank .. and nb*512 + 256 + 128*rank ..), 16 KB apart.
+__device__ __forceinline__ void load_dh_wide_stage(const GemmParams& p, uint32_t a_dst, uint32_t b_dst,
+                                                   uint32_t full, int m_blk, int nbw, int k0, uint32_t rank) {
+  ptx::tma_load_3d_pair(a_dst, &p.tmA, 0, m_blk * BM, k0 / BK, full);
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int j = 0; j < BN_HALF / 64; ++j)
+      ptx::tma_load_2d_pair(b_dst + h * B_BYTES + j * 8192, &p.tmB,
+                            nbw * 2 * BN + h * BN + static_cast<int>(rank) * BN_HALF + j * 64, k0, full);
+}
+
+// Stage ring of one role (producer or MMA issuer).  Each stage's barriers keep
+// their own phase (bit i of `parity` is the parity of the next use of stage i),
+// so the ring can be re-cut: NSTAGE stages of STAGE_BYTES, or WIDE_NSTAGE
+// stages of WIDE_STAGE_BYTES for wide dH tiles, over the same shared memory.
+struct Ring {
+  uint32_t stage = 0, parity = 0, used = 0;
+  int nst = NSTAGE;
+  __device__ __forceinline__ uint32_t stage_bytes() const {
+    return nst == NSTAGE ? static_cast<uint32_t>(STAGE_BYTES) : static_cast<uint32_t>(WIDE_STAGE_BYTES);
   }
-  // The even CTA's stage barriers count both CTAs' loads: waiting on the
-  // last-armed phase of each stage means no TMA write of either CTA is in
-  // flight.  (The odd CTA's loads are consumed by the same MMAs.)
-  __device__ __forceinline__ void drain(const SmemLayout& s, uint32_t rank) const {
-    if (rank != 0) return;
-    for (int i = 0; i < NSTAGE; ++i)
-      if (issued_mask & (1u << i))
-        ptx::wait_bounded(bar_full(s, i), (issued_parity >> i) & 1u, kDrainTimeoutNs, nullptr);
+  __device__ __forceinline__ uint32_t parity_of(uint32_t i) const { return (parity >> i) & 1u; }
+  __device__ __forceinline__ void advance() {
+    used |= 1u << stage;
+    parity ^= 1u << stage;
+    if (++stage == static_cast<uint32_t>(nst)) stage = 0;
   }
 };
 
-// Loads the K blocks of one tile; `kind` 0 = logits, 1 = dH, 2 = dW.
-__device__ __forceinline__ bool produce_tile(const GemmParams& p, const SmemLayout& s, ProducerState& ps, int kind,
+// The producer's side: before the ring is re-cut, every load it issued must
+// have been consumed (the MMAs released the stage), since the new stages
+// overlap the old ones.  Returns false when a wait ran out.
+__device__ __forceinline__ bool producer_recut(const GemmParams& p, const SmemLayout& s, Ring& r, int nst) {
+  if (r.nst == nst) return true;
+  for (uint32_t i = 0; i < static_cast<uint32_t>(r.nst); ++i)
+    if (r.used & (1u << i))
+      if (!ptx::wait_bounded_cluster(bar_empty(s, i), r.parity_of(i) ^ 1u, p.timeout_ns, s.abort_flag)) {
+        abort_cta(p, s);
+        return false;
+      }
+  r.nst = nst;
+  r.stage = 0;
+  return true;
+}
+
+// The MMA issuer's side of a re-cut (it has consumed every stage it waited on).
+__device__ __forceinline__ void mma_recut(Ring& r, int nst) {
+  if (r.nst == nst) return;
+  r.nst = nst;
+  r.stage = 0;
+}
+
+// The even CTA's stage barriers count both CTAs' loads: waiting on the
+// last-armed phase of each stage means no TMA write of either CTA is in
+// flight.  (The odd CTA's loads are consumed by the same MMAs.)
+__device__ __forceinline__ void producer_drain(const SmemLayout& s, const Ring& r, uint32_t rank) {
+  if (rank != 0) return;
+  for (uint32_t i = 0; i < static_cast<uint32_t>(NSTAGE); ++i)
+    if (r.used & (1u << i)) ptx::wait_bounded(bar_full(s, i), r.parity_of(i) ^ 1u, kDrainTimeoutNs, nullptr);
+}
+
+// Loads the K blocks of one tile; `kind` 0 = logits, 1 = dH, 2 = dW, 3 = wide dH
+// (the ring must be cut for the kind: WIDE_NSTAGE stages for 3, NSTAGE otherwise).
+__device__ __forceinline__ bool produce_tile(const GemmParams& p, const SmemLayout& s, Ring& ps, int kind,
                                              int m_blk, int nb, int num_k, uint32_t rank) {
+  const uint32_t tx = kind == 3 ? WIDE_PAIR_TX_BYTES : PAIR_TX_BYTES;
   for (int kb = 0; kb < num_k; ++kb) {
-    if (!ptx::wait_bounded_cluster(bar_empty(s, ps.stage), ps.phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+    if (!ptx::wait_bounded_cluster(bar_empty(s, ps.stage), ps.parity_of(ps.stage) ^ 1u, p.timeout_ns,
+                                   s.abort_flag)) {
       abort_cta(p, s);
       return false;
     }
     const uint32_t full_local = bar_full(s, ps.stage);
-    if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, PAIR_TX_BYTES);
+    if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, tx);
     const uint32_t full = ptx::mapa(full_local, 0);
-    const uint32_t a_dst = ptx::smem_u32(s.stages + ps.stage * STAGE_BYTES);
+    const uint32_t a_dst = ptx::smem_u32(s.stages + ps.stage * ps.stage_bytes());
     const uint32_t b_dst = a_dst + A_BYTES;
     const int k0 = kb * BK;
     if (kind == 0)
       load_logits_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
     else if (kind == 1)
       load_dh_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
-    else
+    else if (kind == 2)
       load_dw_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
+    else
+      load_dh_wide_stage(p, a_dst, b_dst, full, m_blk, nb, k0, rank);
     ps.advance();
   }
   return true;
@@ -368,15 +430,14 @@ __device__ __forceinline__ bool produce_tile(const GemmParams& p, const SmemLayo
 // row, 8-row groups 1024 bytes apart.  MN-major operand: the slice is 16 rows
 // (2048 bytes) further, 64-wide MN blocks 8 KB apart.
 __device__ __forceinline__ bool mma_tile(const GemmParams& p, const SmemLayout& s, uint32_t d_tmem, int num_k,
-                                         uint32_t a_mn, uint32_t b_mn, uint32_t idesc, uint32_t& stage,
-                                         uint32_t& phase) {
+                                         uint32_t a_mn, uint32_t b_mn, uint32_t idesc, Ring& r) {
   for (int kb = 0; kb < num_k; ++kb) {
-    if (!ptx::wait_bounded(bar_full(s, stage), phase, p.timeout_ns, s.abort_flag)) {
+    if (!ptx::wait_bounded(bar_full(s, r.stage), r.parity_of(r.stage), p.timeout_ns, s.abort_flag)) {
       abort_cta(p, s);
       return false;
     }
     ptx::tc_fence_after();
-    const uint32_t a_addr = ptx::smem_u32(s.stages + stage * STAGE_BYTES);
+    const uint32_t a_addr = ptx::smem_u32(s.stages + r.stage * r.stage_bytes());
     const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k) {
@@ -386,11 +447,34 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const SmemLayout& 
                                    : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
       ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
     }
-    ptx::mma_commit_pair(bar_empty(s, stage), 0x3);
-    if (++stage == NSTAGE) {
-      stage = 0;
-      phase ^= 1u;
+    ptx::mma_commit_pair(bar_empty(s, r.stage), 0x3);
+    r.advance();
+  }
+  return true;
+}
+
+// Wide dH tile: per 16-deep slice, the K-major A slice is multiplied with both
+// MN-major B halves, into the accumulators at d0 (hidden columns 0..255 of the
+// 512) and d1 (256..511).
+__device__ __forceinline__ bool mma_tile_wide(const GemmParams& p, const SmemLayout& s, uint32_t d0, uint32_t d1,
+                                              int num_k, uint32_t idesc, Ring& r) {
+  for (int kb = 0; kb < num_k; ++kb) {
+    if (!ptx::wait_bounded(bar_full(s, r.stage), r.parity_of(r.stage), p.timeout_ns, s.abort_flag)) {
+      abort_cta(p, s);
+      return false;
     }
+    ptx::tc_fence_after();
+    const uint32_t a_addr = ptx::smem_u32(s.stages + r.stage * r.stage_bytes());
+    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+      const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+      ptx::mma_bf16_pair(d0, a_desc, ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024), idesc, acc);
+      ptx::mma_bf16_pair(d1, a_desc, ptx::smem_desc_sw128(b_addr + B_BYTES + k * 2048, 8192, 1024), idesc, acc);
+    }
+    ptx::mma_commit_pair(bar_empty(s, r.stage), 0x3);
+    r.advance();
   }
   return true;
 }
@@ -498,14 +582,14 @@ __device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce,
 template <int MODE>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
                                               uint32_t rank) {
-  ProducerState ps;
+  Ring ps;
   bool ok = true;
   for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
     const Unit un = decode_unit<MODE>(p, c, u, rank);
     for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb)
       ok = produce_tile(p, s, ps, 0, un.m_blk, nb, p.num_k_blocks, rank);
   }
-  ps.drain(s, rank);
+  producer_drain(s, ps, rank);
 }
 
 // Even CTA only.
@@ -513,7 +597,8 @@ template <int MODE>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
                                          uint32_t tmem_base) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN, 0, 0);
-  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  Ring ring;
+  uint32_t acc = 0, acc_phase = 0;
   bool ok = true;
   for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
     const Unit un = decode_unit<MODE>(p, c, u, 0);
@@ -524,7 +609,7 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, const Counts& c, c
         break;
       }
       ptx::tc_fence_after();
-      ok = mma_tile(p, s, tmem_base + acc * BN, p.num_k_blocks, 0, 0, idesc, stage, phase);
+      ok = mma_tile(p, s, tmem_base + acc * BN, p.num_k_blocks, 0, 0, idesc, ring);
       if (!ok) break;
       ptx::mma_commit_pair(bar_tfull(s, acc), 0x3);
       acc ^= 1u;
@@ -671,7 +756,7 @@ __device__ __forceinline__ uint32_t ring_addr(const SmemLayout& s, int slot) {
 
 __device__ __forceinline__ void dhw_producer(const GemmParams& p, const Counts& c, const SmemLayout& s,
                                              uint32_t rank) {
-  ProducerState ps;
+  Ring ps;
   const int total = c.n_dh_tiles + p.n_dw_tiles;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
@@ -697,9 +782,12 @@ __device__ __forceinline__ void dhw_producer(const GemmParams& p, const Counts& 
     }
     if (t >= total) break;
     const Tile ti = decode_dhw(p, c, t, rank);
-    if (!produce_tile(p, s, ps, 1 + ti.family, ti.m_blk, ti.nb, ti.num_k, rank)) break;
+    // Wide dH tiles (all first in the tile order) use the ring cut in WIDE_NSTAGE
+    // stages; the first dW tile after them re-cuts it, once per launch.
+    if (!producer_recut(p, s, ps, ti.wide ? WIDE_NSTAGE : NSTAGE)) break;
+    if (!produce_tile(p, s, ps, ti.wide ? 3 : 1 + ti.family, ti.m_blk, ti.nb, ti.num_k, rank)) break;
   }
-  ps.drain(s, rank);
+  producer_drain(s, ps, rank);
 }
 
 // Even CTA only.
@@ -708,7 +796,10 @@ __device__ __forceinline__ void dhw_mma(const GemmParams& p, const Counts& c, co
   constexpr uint32_t idesc_dh = ptx::idesc_bf16_f32(2 * BM, BN, 0, 1);
   constexpr uint32_t idesc_dw = ptx::idesc_bf16_f32(2 * BM, BN, 1, 1);
   const int total = c.n_dh_tiles + p.n_dw_tiles;
-  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  Ring ring;
+  // Accumulator uses so far: use n is buffer n % 2 with phase (n / 2) % 2.  A wide
+  // dH tile takes two consecutive uses (both buffers), a 256-column tile one.
+  uint32_t n_acc = 0;
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
     const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
@@ -720,17 +811,29 @@ __device__ __forceinline__ void dhw_mma(const GemmParams& p, const Counts& c, co
     ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     if (t >= total) break;
     const Tile ti = decode_dhw(p, c, t, 0);
-    if (!ptx::wait_bounded_cluster(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
+    const int uses = ti.wide ? 2 : 1;
+    bool ok = true;
+    for (int h = 0; h < uses && ok; ++h) {
+      const uint32_t n = n_acc + h;
+      ok = ptx::wait_bounded_cluster(bar_tempty(s, n & 1u), ((n >> 1) & 1u) ^ 1u, p.timeout_ns, s.abort_flag);
+    }
+    if (!ok) {
       abort_cta(p, s);
       break;
     }
     ptx::tc_fence_after();
-    if (!mma_tile(p, s, tmem_base + acc * BN, ti.num_k, static_cast<uint32_t>(ti.family), 1u,
-                  ti.family ? idesc_dw : idesc_dh, stage, phase))
-      break;
-    ptx::mma_commit_pair(bar_tfull(s, acc), 0x3);
-    acc ^= 1u;
-    if (acc == 0) acc_phase ^= 1u;
+    mma_recut(ring, ti.wide ? WIDE_NSTAGE : NSTAGE);
+    const uint32_t d0 = tmem_base + (n_acc & 1u) * BN;
+    if (ti.wide) {
+      const uint32_t d1 = tmem_base + ((n_acc + 1) & 1u) * BN;
+      if (!mma_tile_wide(p, s, d0, d1, ti.num_k, idesc_dh, ring)) break;
+    } else {
+      if (!mma_tile(p, s, d0, ti.num_k, static_cast<uint32_t>(ti.family), 1u, ti.family ? idesc_dw : idesc_dh,
+                    ring))
+        break;
+    }
+    for (int h = 0; h < uses; ++h) ptx::mma_commit_pair(bar_tfull(s, (n_acc + h) & 1u), 0x3);
+    n_acc += uses;
   }
   ptx::mma_commit_pair(bar_drain(s), 0x1);
   ptx::wait_bounded(bar_drain(s), 0, kDrainTimeoutNs, nullptr);
@@ -742,7 +845,7 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const Counts& 
   const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
   const int total = c.n_dh_tiles + p.n_dw_tiles;
-  uint32_t acc = 0, acc_phase = 0, box_count = 0;
+  uint32_t n_acc = 0, box_count = 0;  // accumulator uses, as in dhw_mma
   for (int i = 0;; ++i) {
     const int slot = i % kTileRing;
     const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
@@ -755,24 +858,35 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const Counts& 
     if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
     if (t >= total) break;
     const Tile ti = decode_dhw(p, c, t, rank);
-    if (!ptx::wait_bounded_cluster(bar_tfull(s, acc), acc_phase, p.timeout_ns, s.abort_flag)) {
+    const int uses = ti.wide ? 2 : 1;
+    bool ok = true;
+    // One 256-column accumulator at a time: a wide tile's second half is read
+    // after its first half has been stored and released.
+    for (int h = 0; h < uses && ok; ++h) {
+      const uint32_t n = n_acc + h;
+      if (!ptx::wait_bounded_cluster(bar_tfull(s, n & 1u), (n >> 1) & 1u, p.timeout_ns, s.abort_flag)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t tcol = lane_addr + (n & 1u) * BN;
+      if (ti.family == 0) {
+        const int x0 = ti.wide ? ti.nb * 2 * BN + h * BN : ti.nb * BN;
+        if (ti.m_blk * BM < c.rows)
+          epi_bf16_tile<false>(&p.tmOut, tcol, x0, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count, lane, 0.0f,
+                               0.0f, -1);
+      } else {
+        if (ti.m_blk * BM < p.V)
+          epi_f32_tile(&p.tmOut2, p.reduce_out != 0, tcol, ti.nb * BN, ti.m_blk * BM + q * 32, staging0,
+                       box_count, lane);
+      }
+      release_accumulator(s, n & 1u, lane);
+    }
+    if (!ok) {
       abort_cta(p, s);
       break;
     }
-    ptx::tc_fence_after();
-    const uint32_t tcol = lane_addr + acc * BN;
-    if (ti.family == 0) {
-      if (ti.m_blk * BM < c.rows)
-        epi_bf16_tile<false>(&p.tmOut, tcol, ti.nb * BN, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count,
-                             lane, 0.0f, 0.0f, -1);
-    } else {
-      if (ti.m_blk * BM < p.V)
-        epi_f32_tile(&p.tmOut2, p.reduce_out != 0, tcol, ti.nb * BN, ti.m_blk * BM + q * 32, staging0, box_count,
-                     lane);
-    }
-    release_accumulator(s, acc, lane);
-    acc ^= 1u;
-    if (acc == 0) acc_phase ^= 1u;
+    n_acc += uses;
   }
   if (lane == 0) ptx::bulk_wait<0>();
   __syncwarp();
