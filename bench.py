@@ -62,14 +62,15 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel, T, Hd, V, chunk=None):
+def traffic_from_profiles(kernel, T, Hd, V, chunk=None, launches_per_step=1):
     """DRAM bytes per launch of `kernel` at T x Hd x V, from the committed ncu summary of
     a smaller case (profiles/traffic.json), if it was taken on the current kernel sources
     (else None).  The backward kernels work on one token chunk per launch; at the same
-    chunk and Hd their tiles, and their DRAM bytes, grow in proportion to V, so the small
-    case's median is scaled by V / V_case.  The forward's traffic does not grow in
-    proportion to its tiles (it depends on which operand blocks stay in L2), so it is not
-    scaled and is reported only for the captured shape itself."""
+    chunk and Hd their traffic grows in proportion to V, so the small case's medians are
+    scaled by V / V_case, the first chunk's (dW stored) and the later chunks' (dW
+    reduce-added) weighted by the run's launches per step.  The forward's traffic does not
+    grow in proportion to its tiles (it depends on which operand blocks stay in L2), so it
+    is reported only for the captured shape itself."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -81,10 +82,13 @@ def traffic_from_profiles(kernel, T, Hd, V, chunk=None):
     rec = data.get("kernels", {}).get(kernel)
     if not rec or case.get("Hd") != Hd:
         return None
-    per_launch = float(rec["per_launch_median"])
     if rec.get("scale") == "V":
-        return per_launch * V / float(case["V"]) if chunk == case.get("chunk") else None
-    return per_launch if (case.get("T"), case.get("V")) == (T, V) else None
+        if chunk != case.get("chunk"):
+            return None
+        n = max(int(launches_per_step), 1)
+        first, later = float(rec["first_chunk"]["median"]), float(rec["later_chunks"]["median"])
+        return (first + (n - 1) * later) / n * V / float(case["V"])
+    return float(rec["median"]) if (case.get("T"), case.get("V")) == (T, V) else None
 
 
 class ClockSampler:
@@ -672,7 +676,8 @@ def run_ours(args):
     ach = (dom["flops"] / dom["launches"]) / (avg_ms / 1000.0) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    traffic = (traffic_from_profiles(dom_name, T, Hd, V, path.config().get("backward_chunk_tokens"))
+    traffic = (traffic_from_profiles(dom_name, T, Hd, V, path.config().get("backward_chunk_tokens"),
+                                     dom["launches"] / args.steps)
                if args.path == "loss" else None)
     kernels = {k: {"launches": v["launches"], "avg_ms": v["total_ms"] / v["launches"],
                    "share": v["total_ms"] / sum(x["total_ms"] for x in kstats.values()),
