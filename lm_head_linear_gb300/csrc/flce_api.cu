@@ -37,6 +37,7 @@ flce_status fail(flce_status st, const char* fmt, ...) {
   } while (0)
 
 constexpr size_t kHeaderBytes = 256;  // status word and spare scalars at the start of each workspace
+constexpr size_t kUnitCounterOff = 32;  // forward header: the logit kernel's work-unit counter (int32, zeroed per call)
 constexpr int kMaxSplit = 16;         // forward: vocab ranges per token block
 constexpr int64_t kDefaultChunk = 8192;
 constexpr int32_t kMaxShards = 64;    // vocab shards one combine call merges
@@ -369,9 +370,9 @@ int64_t default_chunk(int64_t T) {
   return std::min<int64_t>(c, kDefaultChunk);
 }
 
-// Vocab ranges per token pair for the forward: the even count (the forward
-// walks ranges two at a time) whose units spread most evenly over `grid`
-// persistent SM pairs, ties going to fewer ranges; 1 when V has a single tile.
+// Vocab ranges per token pair for the forward: the even count whose units
+// spread most evenly over `grid` persistent SM pairs, ties going to fewer
+// ranges; 1 when V has a single tile.
 int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
   int best = 1;
   double best_eff = -1.0;
@@ -509,6 +510,7 @@ flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, co
   p.best_val = best_val;
   p.best_idx = best_idx;
   p.status = reinterpret_cast<int32_t*>(ws);
+  p.tile_counter = reinterpret_cast<int32_t*>(ws + kUnitCounterOff);  // zeroed with the header by every caller
   p.timeout_ns = wait_limit_ns(Hd);
   p.rows_dev = rows_dev;
   p.row_index = row_index;

@@ -137,7 +137,7 @@ struct GemmParams {
   float* zy;             // MODE_FWD [T] target logit
   float* best_val;       // MODE_SCORE [n_split][part_stride]: largest logit of the row's vocab range
   int32_t* best_idx;     // MODE_SCORE [n_split][part_stride]: its global vocab id (lowest on ties)
-  int32_t* tile_counter; // MODE_DHW: zero before the launch
+  int32_t* tile_counter; // MODE_DHW tiles / forward units handed out so far; zero before the launch
   int32_t* status;
   uint64_t timeout_ns;
   // Over a list of rows (the backward skips rows whose upstream gradient is zero;
@@ -194,19 +194,16 @@ template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const Counts& c, int u, uint32_t rank) {
   Unit r;
   if constexpr (is_forward(MODE)) {
-    // Vocab ranges are taken two at a time (when n_split is even): units
-    // (token pair, range 2g), (token pair, range 2g + 1), next token pair, ...
-    // Pairs running side by side then walk two ranges' W tiles together and
-    // hold half as many H blocks, which keeps both in L2 (forward DRAM reads
-    // 25 GB -> 10 GB at 65,536 x 2048 x 124,160).
-    const int G = (p.n_split % 2 == 0) ? 2 : 1;
-    const int gsz = G * c.num_m_pairs;
-    const int grp = u / gsz;
-    const int rr = u - grp * gsz;
-    const int split = grp * G + rr % G;
+    // Range-major: units (token pair 0, range 0), (1, 0), ..., (last, 0), (0, 1), ...
+    // The units come from the work-index ring in this order, so the pairs
+    // running side by side hold consecutive token pairs of one vocab range and
+    // walk its W tiles together, each W tile shared by all of them in L2
+    // (forward DRAM reads 7.7 GB at 65,536 x 2048 x 124,160, against 13.5 GB
+    // for two ranges side by side and 25 GB for this order strided statically).
+    const int split = u / c.num_m_pairs;
     const int base = p.num_n_blocks / p.n_split;
     const int rem = p.num_n_blocks % p.n_split;
-    r.m_blk = 2 * (rr / G) + static_cast<int>(rank);
+    r.m_blk = 2 * (u - split * c.num_m_pairs) + static_cast<int>(rank);
     r.split = split;
     r.n_lo = split * base + min(split, rem);
     r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
@@ -577,14 +574,75 @@ __device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce,
   }
 }
 
-// ----------------------------------------------------------------------------- MODE_FWD / MODE_DZ loops (static schedule)
-// Pair c of the grid takes units c, c + pairs, c + 2 * pairs, ...
+// ----------------------------------------------------------------------------- work-index ring
+// Dynamic schedule (MODE_DHW tiles, MODE_FWD / MODE_SCORE units): the even CTA's
+// producer takes the next index from the launch's global counter, writes it into
+// slot i % kTileRing of both CTAs' rings and arrives on both CTAs' tile_full
+// barriers; the consumers (the even CTA's MMA thread, the odd CTA's producer and
+// all eight epilogue warps) read their own ring and arrive on the even CTA's
+// tile_empty barrier.  An index past the last one ends every role's loop.  The
+// pairs then work on a contiguous window of the index order at any time, however
+// their speeds differ, which keeps operand blocks they share in L2.
+__device__ __forceinline__ uint32_t ring_addr(const SmemLayout& s, int slot) {
+  return ptx::smem_u32(const_cast<int*>(s.tile_ring + slot));
+}
+
+// The even CTA's producer: claims the i-th index of this pair into *t.
+__device__ __forceinline__ bool ring_claim(const GemmParams& p, const SmemLayout& s, int i, int* t) {
+  const int slot = i % kTileRing;
+  const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
+  if (!ptx::wait_bounded_cluster(bar_tile_empty(s, slot), ph ^ 1u, p.timeout_ns, s.abort_flag)) {
+    abort_cta(p, s);
+    return false;
+  }
+  *t = atomicAdd(p.tile_counter, 1);
+  s.tile_ring[slot] = *t;
+  ptx::st_shared_cluster_u32(ptx::mapa(ring_addr(s, slot), 1), static_cast<uint32_t>(*t));
+  ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_full(s, slot), 0));
+  ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_full(s, slot), 1));
+  return true;
+}
+
+// A consumer: reads the i-th index of this pair into *t and releases the slot
+// (one arrival per calling thread, or per warp through lane 0 with `per_warp`).
+__device__ __forceinline__ bool ring_take(const GemmParams& p, const SmemLayout& s, int i, int* t, bool per_warp,
+                                          int lane) {
+  const int slot = i % kTileRing;
+  const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
+  if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
+    abort_cta(p, s);
+    return false;
+  }
+  *t = s.tile_ring[slot];
+  if (per_warp) __syncwarp();
+  if (!per_warp || lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
+  return true;
+}
+
+// ----------------------------------------------------------------------------- MODE_FWD / MODE_DZ / MODE_SCORE loops
+// Forward units (token pair x vocab range) come from the work-index ring; the
+// dZ recompute's single-tile units are strided statically (pair c takes units
+// c, c + pairs, c + 2 * pairs, ...).
+template <int MODE>
+__device__ __forceinline__ bool next_unit(const GemmParams& p, const SmemLayout& s, int i, int* u, int role,
+                                          uint32_t rank, int lane) {
+  if constexpr (is_forward(MODE)) {
+    // role 0: producer, 1: MMA issuer, 2: epilogue warp
+    if (role == 0 && rank == 0) return ring_claim(p, s, i, u);
+    return ring_take(p, s, i, u, role == 2, lane);
+  } else {
+    *u = static_cast<int>(blockIdx.x >> 1) + i * static_cast<int>(gridDim.x >> 1);
+    return true;
+  }
+}
 template <int MODE>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
                                               uint32_t rank) {
   Ring ps;
   bool ok = true;
-  for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
+  for (int i = 0; ok; ++i) {
+    int u;
+    if (!next_unit<MODE>(p, s, i, &u, 0, rank, 0) || u >= c.num_units) break;
     const Unit un = decode_unit<MODE>(p, c, u, rank);
     for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb)
       ok = produce_tile(p, s, ps, 0, un.m_blk, nb, p.num_k_blocks, rank);
@@ -600,7 +658,9 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, const Counts& c, c
   Ring ring;
   uint32_t acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
+  for (int i = 0; ok; ++i) {
+    int u;
+    if (!next_unit<MODE>(p, s, i, &u, 1, 0, 0) || u >= c.num_units) break;
     const Unit un = decode_unit<MODE>(p, c, u, 0);
     for (int nb = un.n_lo; nb < un.n_hi && ok; ++nb) {
       if (!ptx::wait_bounded_cluster(bar_tempty(s, acc), acc_phase ^ 1u, p.timeout_ns, s.abort_flag)) {
@@ -639,7 +699,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const Counts&
   const uint32_t staging0 = ptx::smem_u32(s.staging + q * 2 * STAGING_BOX_BYTES);
   bool ok = true;
 
-  for (int u = blockIdx.x >> 1; u < c.num_units && ok; u += gridDim.x >> 1) {
+  for (int i = 0; ok; ++i) {
+    int u;
+    if (!next_unit<MODE>(p, s, i, &u, 2, rank, lane) || u >= c.num_units) break;
     const Unit un = decode_unit<MODE>(p, c, u, rank);
     const bool active = un.m_blk * BM < c.rows;       // the odd CTA of a ragged last pair has no rows
     const int t_local = un.m_blk * BM + row_in_tile;  // token within the launch
@@ -744,42 +806,14 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const Counts&
 }
 
 // ----------------------------------------------------------------------------- MODE_DHW loops (dynamic schedule)
-// The even CTA's producer takes the next tile index from the global counter,
-// writes it into slot i % kTileRing of both CTAs' rings and arrives on both
-// CTAs' tile_full barriers; the consumers (the even CTA's MMA thread, the odd
-// CTA's producer and all eight epilogue warps) read their own ring and arrive
-// on the even CTA's tile_empty barrier.  An index >= the tile count ends every
-// role's loop.
-__device__ __forceinline__ uint32_t ring_addr(const SmemLayout& s, int slot) {
-  return ptx::smem_u32(const_cast<int*>(s.tile_ring + slot));
-}
 
 __device__ __forceinline__ void dhw_producer(const GemmParams& p, const Counts& c, const SmemLayout& s,
                                              uint32_t rank) {
   Ring ps;
   const int total = c.n_dh_tiles + p.n_dw_tiles;
   for (int i = 0;; ++i) {
-    const int slot = i % kTileRing;
-    const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
     int t;
-    if (rank == 0) {
-      if (!ptx::wait_bounded_cluster(bar_tile_empty(s, slot), ph ^ 1u, p.timeout_ns, s.abort_flag)) {
-        abort_cta(p, s);
-        break;
-      }
-      t = atomicAdd(p.tile_counter, 1);
-      s.tile_ring[slot] = t;
-      ptx::st_shared_cluster_u32(ptx::mapa(ring_addr(s, slot), 1), static_cast<uint32_t>(t));
-      ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_full(s, slot), 0));
-      ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_full(s, slot), 1));
-    } else {
-      if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
-        abort_cta(p, s);
-        break;
-      }
-      t = s.tile_ring[slot];
-      ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
-    }
+    if (!(rank == 0 ? ring_claim(p, s, i, &t) : ring_take(p, s, i, &t, false, 0))) break;
     if (t >= total) break;
     const Tile ti = decode_dhw(p, c, t, rank);
     // Wide dH tiles (all first in the tile order) use the ring cut in WIDE_NSTAGE
@@ -801,14 +835,8 @@ __device__ __forceinline__ void dhw_mma(const GemmParams& p, const Counts& c, co
   // dH tile takes two consecutive uses (both buffers), a 256-column tile one.
   uint32_t n_acc = 0;
   for (int i = 0;; ++i) {
-    const int slot = i % kTileRing;
-    const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
-    if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
-      abort_cta(p, s);
-      break;
-    }
-    const int t = s.tile_ring[slot];
-    ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
+    int t;
+    if (!ring_take(p, s, i, &t, false, 0)) break;
     if (t >= total) break;
     const Tile ti = decode_dhw(p, c, t, 0);
     const int uses = ti.wide ? 2 : 1;
@@ -847,15 +875,8 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const Counts& 
   const int total = c.n_dh_tiles + p.n_dw_tiles;
   uint32_t n_acc = 0, box_count = 0;  // accumulator uses, as in dhw_mma
   for (int i = 0;; ++i) {
-    const int slot = i % kTileRing;
-    const uint32_t ph = static_cast<uint32_t>(i / kTileRing) & 1u;
-    if (!ptx::wait_bounded_cluster(bar_tile_full(s, slot), ph, p.timeout_ns, s.abort_flag)) {
-      abort_cta(p, s);
-      break;
-    }
-    const int t = s.tile_ring[slot];
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(bar_tile_empty(s, slot), 0));
+    int t;
+    if (!ring_take(p, s, i, &t, true, lane)) break;
     if (t >= total) break;
     const Tile ti = decode_dhw(p, c, t, rank);
     const int uses = ti.wide ? 2 : 1;

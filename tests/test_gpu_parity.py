@@ -72,6 +72,16 @@ def test_many_token_chunks(cuda_device):
     _full_check(inp, run(inp, cuda_device, bwd_workspace_bytes=chunk_ws))
 
 
+def test_wide_dh_tiles_odd_block_count_many_chunks(cuda_device):
+    """Hd = 1536 (three 512-column dH blocks, 256 x 512 dH tiles) over 128-token chunks:
+    each launch cuts its stage ring for the wide tiles and re-cuts it for the dW tiles;
+    most SM pairs get no dH tile and start in the dW cut.  Full oracle parity."""
+    inp = generate("rlpg", T=1000, Hd=1536, V=3000, n_seq=4)
+    chunk_ws = flce.flce_backward_workspace_size_for_chunk(1000, 1536, 3000, 128)
+    assert flce.flce_backward_chunk_tokens(1000, 1536, 3000, chunk_ws) == 128
+    _full_check(inp, run(inp, cuda_device, bwd_workspace_bytes=chunk_ws))
+
+
 def test_deterministic(cuda_device):
     inp = generate("medium", T=1000, Hd=256, V=5000)
     a = run(inp, cuda_device)
