@@ -39,7 +39,13 @@
 // the 128-byte TMA / UMMA swizzle.  Operand halves pass through a ring of
 // NSTAGE shared-memory stages; the accumulator is double-buffered in TMEM
 // (2 x 256 columns) so that the epilogue of one tile overlaps the MMAs of the
-// next.
+// next.  Exception: MODE_DHW's dH tiles are 256 x 512 when Hd allows (two N =
+// 256 MMAs per A slice, both accumulators, the ring re-cut in WIDE_NSTAGE
+// larger stages), which moves fewer operand bytes per FLOP on their long K loop.
+//
+// Work is handed out dynamically for the forward units and the MODE_DHW tiles
+// (a global counter and a small ring in shared memory, see "work-index ring")
+// and statically for the dZ recompute's tiles.
 #pragma once
 
 #include <cstdint>
@@ -157,8 +163,8 @@ struct GemmParams {
 // that follow from the chunk's share of the row list.
 struct Counts {
   int rows;           // rows of the chunk
-  int num_m_pairs;    // 256-row pairs along M (static modes) / dH tiles' token pairs
-  int num_units;      // static modes: work units
+  int num_m_pairs;    // 256-row pairs along M (unit modes) / dH tiles' token pairs
+  int num_units;      // unit modes (forward, scoring, dZ recompute): work units
   int n_dh_tiles;     // MODE_DHW
   int num_k_blocks2;  // MODE_DHW: K blocks of a dW tile
 };
@@ -560,7 +566,7 @@ __device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tc
   }
 }
 
-// fp32 tile store or reduce-add (dW): 8 boxes of 32 columns.
+// fp32 tile store or TMA reduce-add (dW): 8 boxes of 32 columns.
 __device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce, uint32_t tcol, int x0, int yrow,
                                              uint32_t staging0, uint32_t& box_count, int lane) {
 #pragma unroll 1
