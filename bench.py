@@ -632,11 +632,17 @@ def run_ours(args):
 
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # the first input copy is timed on its own stream too: its bandwidth tells a run
+    # whose host copies are slow (a busy host) from one whose kernels are
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(stream)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
+    c0.record(s_in)
     h2d(0)
+    c1.record(s_in)
     for i in range(e2e_steps):
         j = i % 2
         if i + 1 < e2e_steps:
@@ -660,8 +666,10 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))
     h2d_bytes = sum(t.numel() * t.element_size() for t in path.host)
     d2h_bytes = sum(t.numel() * t.element_size() for t in back_h)
+    first_copy_ms = c0.elapsed_time(c1)
     e2e = {"value": whole_job_tokens_per_s(T * e2e_steps, world, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "steps": e2e_steps}
+           "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "steps": e2e_steps,
+           "h2d_gb_per_s_first_copy": (h2d_bytes / first_copy_ms / 1e6) if first_copy_ms else None}
 
     if rank != 0:
         if world > 1:
