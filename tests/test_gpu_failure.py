@@ -65,3 +65,34 @@ def test_gemm_abort_path_reports_timeout(cuda_device):
     small = generate("tiny", T=300, Hd=128, V=1000)
     out = run(small, cuda_device)
     assert out["fwd_status"] == 0 and out["bwd_status"] == 0
+
+
+def test_backward_abort_path_with_wide_dh_tiles_reports_timeout(cuda_device):
+    """The dH+dW kernel's abort path, in a 256 x 512 dH tile (both TMEM accumulators,
+    the stage ring cut for wide tiles).  T = 256, Hd = 512, V = 400,000: the one wide
+    dH tile has a K loop of 6,250 blocks (~3.5 ms of one SM pair) while the other pairs
+    run short dW tiles.  With the wait limit at 1 ms the epilogue's wait for that
+    tile's accumulators runs out: the call reports FLCE_ERR_TIMEOUT through the status
+    word and the context stays usable; with the default limit the same backward
+    matches the oracle."""
+    import oracle
+    from gpu_helpers import TOL_GRAD, rel_fro
+    inp = generate("medium", T=256, Hd=512, V=400000)
+    H, W, y, dl = to_device(inp, cuda_device)
+    _, lse, _, _, fws = flce.flce_forward(H, W, y, inp.ignore_index, inp.reduction)
+    assert flce.flce_read_device_status(fws) == 0
+    try:
+        flce.flce_set_wait_timeout_ns(1_000_000)
+        _, _, bws = flce.flce_backward(dl, H, W, y, lse, inp.ignore_index, inp.reduction)
+        assert flce.flce_read_device_status(bws) == 7
+    finally:
+        flce.flce_set_wait_timeout_ns(4_000_000_000)
+    dH, dW, bws = flce.flce_backward(dl, H, W, y, lse, inp.ignore_index, inp.reduction)
+    assert flce.flce_read_device_status(bws) == 0
+    dH_ref, dW_ref = oracle.backward(inp.dloss, inp.H64(), inp.W64(), inp.targets, inp.ignore_index,
+                                     inp.reduction, row_block=64)
+    assert rel_fro(dH.float().cpu().numpy(), dH_ref) <= TOL_GRAD
+    assert rel_fro(dW.cpu().numpy(), dW_ref) <= TOL_GRAD
+    small = generate("tiny", T=300, Hd=128, V=1000)
+    out = run(small, cuda_device)
+    assert out["fwd_status"] == 0 and out["bwd_status"] == 0
