@@ -59,7 +59,7 @@ extern "C" {
 #endif
 
 /* 1: the first interface.  2: the backward skips rows with a zero upstream
- * weight (its workspace holds the row list and the chunk's H and dH rows),
+ * weight (its workspace holds the row list and the chunk's H rows),
  * flce_forward_valid, flce_score_valid and flce_backward_workspace_size_for_chunk
  * added, kernel kinds 6-8 added to the timing aid. */
 #define FLCE_ABI_VERSION 2
@@ -96,10 +96,10 @@ FLCE_API size_t flce_forward_workspace_size(int64_t T, int64_t Hd, int64_t V);
  * (ignored targets; their dZ rows vanish) and works on chunks of `chunk` of
  * the remaining rows, in token order; the workspace holds one [chunk x V] bf16
  * slice of dZ (the page's [block x vocab] residency), the chunk's rows of H
- * and dH ([chunk x Hd] bf16 each) and O(T) scalars.  The default chunk is T
- * rounded up to 128 for T <= 256, else min(8192, T/2 rounded down to 128), so
- * for T > 256 and Hd < V/2 the workspace stays below the T*V*2 bytes of one
- * dense bf16 logits tensor.  A larger or smaller workspace is accepted:
+ * ([chunk x Hd] bf16) and O(T) scalars.  The default chunk is T rounded up to
+ * 128 for T <= 256, else min(8192, T/2 rounded down to 128), so for T > 256 and
+ * Hd < V/2 the workspace stays below the T*V*2 bytes of one dense bf16 logits
+ * tensor.  A larger or smaller workspace is accepted:
  * the backward then uses the largest chunk (a multiple of 128 rows, at least
  * 128) that fits. */
 FLCE_API size_t flce_backward_workspace_size(int64_t T, int64_t Hd, int64_t V);
@@ -332,7 +332,7 @@ typedef enum flce_kernel_kind {
   FLCE_KERNEL_BWD_DZ = 4,         /* recomputed logit tiles + dZ epilogue, bf16 dZ chunk */
   FLCE_KERNEL_BWD_DH_DW = 5,      /* dH chunk = dZ W and dW (+)= dZ^T H, one launch per chunk */
   FLCE_KERNEL_BWD_GATHER = 6,     /* the chunk's rows of H gathered through the row list */
-  FLCE_KERNEL_BWD_SCATTER = 7,    /* the chunk's dH rows written back to their tokens */
+  FLCE_KERNEL_BWD_SCATTER = 7,    /* not launched: the dH tiles write their rows straight to their tokens */
   FLCE_KERNEL_FWD_LIST = 8,       /* flce_forward_valid: the list of rows with a valid target */
   FLCE_KERNEL_KINDS = 9
 } flce_kernel_kind;

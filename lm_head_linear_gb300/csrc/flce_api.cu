@@ -330,14 +330,14 @@ struct BwdLayout {
   int64_t chunk;
   int64_t v_pad;
   int64_t max_chunks;
-  size_t cnt_off, g_off, idx_off, hc_off, dhc_off, dz_off, total;
+  size_t cnt_off, g_off, idx_off, hc_off, dz_off, total;
 };
 
 constexpr size_t kRowCountOff = 16;  // backward header: length of the row list (int32)
 
 // Header (status word, row count) | tile counters (one per possible chunk) |
-// g [T] | row list [T] | H rows of the chunk [chunk, Hd] | dH rows of the chunk
-// [chunk, Hd] | dZ chunk: V_pad / 64 panels of [chunk, 64] (DzPanels).
+// g [T] | row list [T] | H rows of the chunk [chunk, Hd] | dZ chunk: V_pad / 64
+// panels of [chunk, 64] (DzPanels).  The dH rows go straight to the caller's dH.
 BwdLayout bwd_layout(int64_t T, int64_t Hd, int64_t V, int64_t chunk) {
   BwdLayout L{};
   L.chunk = chunk;
@@ -352,8 +352,6 @@ BwdLayout bwd_layout(int64_t T, int64_t Hd, int64_t V, int64_t chunk) {
   L.idx_off = off;
   off = align_up(off + sizeof(int32_t) * t1, 1024);
   L.hc_off = off;
-  off = align_up(off + 2ull * static_cast<size_t>(chunk) * static_cast<size_t>(Hd), 1024);
-  L.dhc_off = off;
   off = align_up(off + 2ull * static_cast<size_t>(chunk) * static_cast<size_t>(Hd), 1024);
   L.dz_off = off;
   off = align_up(off + 2ull * static_cast<size_t>(chunk) * L.v_pad, 256);
@@ -616,7 +614,6 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
   int32_t* row_index = reinterpret_cast<int32_t*>(ws + L.idx_off);
   int32_t* row_count = reinterpret_cast<int32_t*>(ws + kRowCountOff);
   void* Hc = ws + L.hc_off;
-  void* dHc = ws + L.dhc_off;
   void* dz = ws + L.dz_off;
 
   // Rows whose g_t is zero have zero dZ rows: their dH rows are zero and they add
@@ -631,12 +628,11 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     if ((st = check_launch("bwd_prep")) != FLCE_OK) return st;
   }
   const int64_t n_hd_blocks = cdiv(Hd, BN);
-  CUtensorMap tm_Hc_k, tm_W_k, tm_W_mn, tm_Hc_mn, tm_dHc, tm_dW_out, tm_dz_store, tm_dz_k, tm_dz_mn;
+  CUtensorMap tm_Hc_k, tm_W_k, tm_W_mn, tm_Hc_mn, tm_dW_out, tm_dz_store, tm_dz_k, tm_dz_mn;
   if ((st = make_map(&tm_Hc_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hc, Hd, chunk, Hd * 2, BK, BM)) != FLCE_OK) return st;
   if ((st = make_map(&tm_W_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, BK, BN_HALF)) != FLCE_OK) return st;
   if ((st = make_map(&tm_W_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, Hd, V, Hd * 2, 64, 64)) != FLCE_OK) return st;
   if ((st = make_map(&tm_Hc_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hc, Hd, chunk, Hd * 2, 64, 64)) != FLCE_OK) return st;
-  if ((st = make_map(&tm_dHc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dHc, Hd, chunk, Hd * 2, 64, 32)) != FLCE_OK) return st;
   if ((st = make_map(&tm_dW_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, Hd, V, Hd * 4, 32, 32)) != FLCE_OK) return st;
   // dZ block: V_pad / 64 panels of [chunk x 64] (the kernels' DzPanels layout)
   const uint64_t dz_panels = static_cast<uint64_t>(L.v_pad / 64);
@@ -701,7 +697,6 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     //     the first chunk stores dW, later chunks add to it, in chunk order.
     p.tmA = tm_dz_k;
     p.tmB = tm_W_mn;
-    p.tmOut = tm_dHc;
     p.tmA2 = tm_dz_mn;
     p.tmB2 = tm_Hc_mn;
     p.tmOut2 = tm_dW_out;
@@ -716,6 +711,9 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
     p.n_dw_tiles = static_cast<int32_t>(cdiv(V, 2 * BM) * n_hd_blocks);
     p.reduce_out = c > 0 ? 1 : 0;
     p.tile_counter = counters + c;
+    p.dH_out = static_cast<uint16_t*>(dH);
+    p.dH_ld = Hd;
+    p.Hd = static_cast<int32_t>(Hd);
     p.dW_zero = dW;
     p.dW_elems = V * Hd;
     // dH tiles: K = V (twice the work per unit of K when wide); dW tiles: K = the chunk
@@ -727,14 +725,6 @@ flce_status backward_impl(const float* dloss, const float* dlogp, const void* H,
       gemm_kernel<MODE_DHW><<<grid, kThreads, smem_bytes_for(MODE_DHW), s>>>(p);
       ks.done();
       if ((st = check_launch("bwd_dh_dw")) != FLCE_OK) return st;
-    }
-    {
-      KernelScope ks(FLCE_KERNEL_BWD_SCATTER, s, 0.0, 0.0, row_count, c0, chunk, 0.0, 4.0 * Hd + 4.0);
-      scatter_rows_kernel<<<copy_grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(dHc), row_index, row_count,
-                                                             static_cast<int>(c0), static_cast<int>(chunk), row_vecs,
-                                                             static_cast<uint4*>(dH));
-      ks.done();
-      if ((st = check_launch("bwd_scatter")) != FLCE_OK) return st;
     }
   }
   return FLCE_OK;
@@ -851,9 +841,9 @@ int64_t flce_backward_chunk_tokens(int64_t T, int64_t Hd, int64_t V, size_t work
   const int64_t cap = static_cast<int64_t>(align_up(static_cast<size_t>(std::max<int64_t>(T, 1)), 128));
   const BwdLayout L0 = bwd_layout(T, Hd, V, 0);
   if (workspace_bytes < L0.total) return 0;
-  // per chunk row: its dZ row, its H row and its dH row; the regions' alignment
-  // padding (a few KB) can cost one step of 128 rows
-  const size_t per_row = 2ull * static_cast<size_t>(L0.v_pad) + 4ull * static_cast<size_t>(Hd);
+  // per chunk row: its dZ row and its H row; the regions' alignment padding (a
+  // few KB) can cost one step of 128 rows
+  const size_t per_row = 2ull * static_cast<size_t>(L0.v_pad) + 2ull * static_cast<size_t>(Hd);
   int64_t c = static_cast<int64_t>((workspace_bytes - L0.hc_off) / per_row);
   c = std::min(c / 128 * 128, cap);
   while (c >= 128 && bwd_layout(T, Hd, V, c).total > workspace_bytes) c -= 128;

@@ -111,7 +111,7 @@ static_assert(kBarriers * 8 + 8 + kTileRing * 4 <= kSmemTail, "smem tail");
 // rows 2 V bytes apart.
 struct GemmParams {
   // MODE_FWD / MODE_DZ: A = H (K-major), B = W (K-major), tmOut = dZ store (panels).
-  // MODE_DHW dH tiles: A = dZ (K-major, panels), B = W (MN-major), tmOut = dH store.
+  // MODE_DHW dH tiles: A = dZ (K-major, panels), B = W (MN-major); dH written through dH_out.
   CUtensorMap tmA;
   CUtensorMap tmB;
   CUtensorMap tmOut;
@@ -155,6 +155,9 @@ struct GemmParams {
   const int32_t* rows_dev;
   const int32_t* row_index;
   int32_t index0;
+  uint16_t* dH_out;      // MODE_DHW: dH [T, Hd] bf16 (row stride dH_ld elements); dH tiles write their
+  int64_t dH_ld;         //   rows straight to their tokens' rows through the row list
+  int32_t Hd;
   float* dW_zero;        // MODE_DHW: dW, zero-filled here when the list is empty
   int64_t dW_elems;
 };
@@ -566,6 +569,45 @@ __device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tc
   }
 }
 
+// bf16 dH tile rows (256 columns from x0) written straight to their tokens' rows
+// of dH: lane l of the warp holds chunk row l, whose token is `token` (< 0: no
+// row).  Each 64-column piece is staged (one row per lane, 128-byte swizzle) and
+// read back four rows per instruction, 8 lanes per 128-byte row segment, so every
+// store covers whole segments.  Columns >= Hd are not written.
+__device__ __forceinline__ void epi_dh_rows(uint16_t* dH, int64_t ld, int Hd, int token, uint32_t tcol, int x0,
+                                            uint32_t staging0, uint32_t& box_count, int lane) {
+  const int sub = lane >> 3;   // row within a group of four
+  const int piece = lane & 7;  // 16-byte piece of the row segment
+  // The staging buffers may still be read by this warp's TMA stores of a dW tile.
+  if (lane == 0) ptx::bulk_wait_read<0>();
+  __syncwarp();
+#pragma unroll 1
+  for (int j = 0; j < BN / 64; ++j) {
+    uint32_t w[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float v[32];
+      tmem_load32_sync(tcol + j * 64 + h * 32, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[h * 16 + i] = ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+    const uint32_t buf = staging0 + (box_count & 1u) * STAGING_BOX_BYTES;
+    __syncwarp();
+    stage_row_words(buf, lane, w);
+    __syncwarp();
+    const int col = x0 + j * 64 + piece * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + sub;
+      const int tok = __shfl_sync(0xffffffffu, token, r);
+      uint32_t a, b, c, d;
+      ptx::ld_shared_v4(buf + r * 128 + ((piece ^ (r & 7)) << 4), a, b, c, d);
+      if (tok >= 0 && col < Hd) ptx::st_global_v4(dH + static_cast<int64_t>(tok) * ld + col, a, b, c, d);
+    }
+    ++box_count;
+  }
+}
+
 // fp32 tile store or TMA reduce-add (dW): 8 boxes of 32 columns.
 __device__ __forceinline__ void epi_f32_tile(const CUtensorMap* tm, bool reduce, uint32_t tcol, int x0, int yrow,
                                              uint32_t staging0, uint32_t& box_count, int lane) {
@@ -899,9 +941,11 @@ __device__ __forceinline__ void dhw_epilogue(const GemmParams& p, const Counts& 
       const uint32_t tcol = lane_addr + (n & 1u) * BN;
       if (ti.family == 0) {
         const int x0 = ti.wide ? ti.nb * 2 * BN + h * BN : ti.nb * BN;
-        if (ti.m_blk * BM < c.rows)
-          epi_bf16_tile<false>(&p.tmOut, tcol, x0, p.row0 + ti.m_blk * BM + q * 32, staging0, box_count, lane, 0.0f,
-                               0.0f, -1);
+        if (ti.m_blk * BM < c.rows) {
+          const int r = ti.m_blk * BM + q * 32 + lane;  // row of the chunk
+          const int token = r < c.rows ? (p.row_index ? p.row_index[p.index0 + r] : p.row0 + r) : -1;
+          epi_dh_rows(p.dH_out, p.dH_ld, p.Hd, token, tcol, x0, staging0, box_count, lane);
+        }
       } else {
         if (ti.m_blk * BM < p.V)
           epi_f32_tile(&p.tmOut2, p.reduce_out != 0, tcol, ti.nb * BN, ti.m_blk * BM + q * 32, staging0,
@@ -969,7 +1013,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&p.tmA);
     ptx::prefetch_tmap(&p.tmB);
-    if (!is_forward(MODE)) ptx::prefetch_tmap(&p.tmOut);
+    if (MODE == MODE_DZ) ptx::prefetch_tmap(&p.tmOut);
     if (MODE == MODE_DHW) {
       ptx::prefetch_tmap(&p.tmA2);
       ptx::prefetch_tmap(&p.tmB2);
@@ -1364,20 +1408,6 @@ __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(const uint4* 
     const int i = static_cast<int>(v / row_vecs);
     const int j = static_cast<int>(v - static_cast<int64_t>(i) * row_vecs);
     Hc[v] = i < rows ? H[static_cast<int64_t>(row_index[index0 + i]) * row_vecs + j] : make_uint4(0, 0, 0, 0);
-  }
-}
-
-// dH rows of the chunk (list order, in dHc) written back to their tokens' rows.
-__global__ void __launch_bounds__(kCopyThreads) scatter_rows_kernel(const uint4* dHc, const int32_t* row_index,
-                                                                    const int32_t* row_count, int index0, int cap,
-                                                                    int row_vecs, uint4* dH) {
-  const int rows = min(max(*row_count - index0, 0), cap);
-  const int64_t n = static_cast<int64_t>(rows) * row_vecs;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n; v += stride) {
-    const int i = static_cast<int>(v / row_vecs);
-    const int j = static_cast<int>(v - static_cast<int64_t>(i) * row_vecs);
-    dH[static_cast<int64_t>(row_index[index0 + i]) * row_vecs + j] = dHc[v];
   }
 }
 

@@ -240,8 +240,8 @@ def test_full_size_workload(name, cuda_device):
     bws_b = flce.flce_backward_workspace_size(T, Hd, V)
     chunk = flce.flce_backward_chunk_tokens(T, Hd, V, bws_b)
     v_pad = (V + 63) // 64 * 64
-    # dZ slice [chunk x V], the chunk's H and dH rows [chunk x Hd] each, g and the row list [T]
-    assert bws_b <= 2 * chunk * v_pad + 4 * chunk * Hd + 8 * T + (1 << 20)
+    # dZ slice [chunk x V], the chunk's H rows [chunk x Hd], g and the row list [T]
+    assert bws_b <= 2 * chunk * v_pad + 2 * chunk * Hd + 8 * T + (1 << 20)
     assert fws_b <= (8 * 16 + 4) * (T + 128) + (1 << 20)  # (m, s) per token and vocab range, at most 16 ranges
     io = 2 * T * Hd + 2 * V * Hd + 8 * T + 4 * T + 3 * 4 * T + 8 + 2 * T * Hd + 4 * V * Hd
     assert peak_extra <= io + fws_b + bws_b + (64 << 20)  # caching-allocator rounding
