@@ -389,6 +389,21 @@ int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
   return best;
 }
 
+// The forward's unit schedule: range-major units from the work-index ring when
+// the H blocks of all in-flight token pairs (pairs of them, 512 * Hd bytes each)
+// fit in about 80 MB of L2, else units strided over the pairs with the vocab
+// ranges taken two at a time (when n_split is even).  Both from measurements at
+// Hd = 2048 and 4096 (see the kernel's decode_unit).
+struct FwdSchedule {
+  int split_group;
+  int dynamic;
+};
+FwdSchedule fwd_schedule(int n_split, int64_t Hd, int64_t pairs) {
+  constexpr double kL2Budget = 80.0 * 1024 * 1024;
+  if (static_cast<double>(pairs) * 512.0 * static_cast<double>(Hd) <= kL2Budget) return {1, 1};
+  return {n_split % 2 == 0 ? 2 : 1, 0};
+}
+
 flce_status check_common(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,
                          int64_t ignore_index, int32_t reduction) {
   if (T < 0 || T >= kMaxRows) return fail(FLCE_ERR_INVALID_ARG, "T = %lld out of range", (long long)T);
@@ -494,6 +509,9 @@ flce_status launch_logits_lse(DeviceInfo* dev, cudaStream_t s, const void* H, co
   p.num_n_blocks = static_cast<int32_t>(n_blocks);
   p.num_k_blocks = static_cast<int32_t>(Hd / BK);
   p.n_split = n_split;
+  const FwdSchedule sched = fwd_schedule(n_split, Hd, std::min<int64_t>(dev->pairs[MODE_FWD], m_pairs * n_split));
+  p.split_group = sched.split_group;
+  p.dynamic_units = sched.dynamic;
   p.num_units = static_cast<int32_t>(m_pairs * n_split);
   p.row0 = 0;
   p.rows = static_cast<int32_t>(T);

@@ -123,6 +123,8 @@ struct GemmParams {
   int32_t num_n_blocks;
   int32_t num_k_blocks;
   int32_t n_split;       // MODE_FWD: vocab ranges per token block
+  int32_t split_group;   // MODE_FWD: vocab ranges side by side in the unit order (divides n_split)
+  int32_t dynamic_units; // MODE_FWD: 1 = units from the work-index ring, 0 = strided over the pairs
   int32_t num_units;
   int32_t row0;          // first row of the launch in the A / B2 operand maps (0 for MODE_FWD)
   int32_t rows;          // rows of the launch (T for MODE_FWD); over a row list: the chunk's capacity
@@ -203,16 +205,26 @@ template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const Counts& c, int u, uint32_t rank) {
   Unit r;
   if constexpr (is_forward(MODE)) {
-    // Range-major: units (token pair 0, range 0), (1, 0), ..., (last, 0), (0, 1), ...
-    // The units come from the work-index ring in this order, so the pairs
-    // running side by side hold consecutive token pairs of one vocab range and
-    // walk its W tiles together, each W tile shared by all of them in L2
-    // (forward DRAM reads 7.7 GB at 65,536 x 2048 x 124,160, against 13.5 GB
-    // for two ranges side by side and 25 GB for this order strided statically).
-    const int split = u / c.num_m_pairs;
+    // Units in groups of G = p.split_group vocab ranges: (token pair 0, range
+    // 0 .. G-1), (token pair 1, range 0 .. G-1), ..., then the next G ranges.
+    // Two schedules (chosen on the host from measurements):
+    //  * range-major (G = 1) with the units from the work-index ring, when the
+    //    in-flight pairs' H blocks (512 * Hd bytes each) fit in L2: the pairs
+    //    then hold consecutive token pairs of one range and share each W tile
+    //    (forward DRAM reads 5.5-7.7 GB at 65,536 x 2048 x 124,160, against
+    //    13.5-14.5 GB with G = 2);
+    //  * otherwise G = 2 with the units strided over the pairs (pair c takes
+    //    units c, c + pairs, ...), which puts the two units sharing an H block
+    //    on neighbouring clusters (at 131,072 x 4096 x 124,160 the forward takes
+    //    81 ms so, against 86-90 ms from the ring with G = 1, 2 or 4).
+    const int G = p.split_group;
+    const int gsz = G * c.num_m_pairs;
+    const int grp = u / gsz;
+    const int rr = u - grp * gsz;
+    const int split = grp * G + rr % G;
     const int base = p.num_n_blocks / p.n_split;
     const int rem = p.num_n_blocks % p.n_split;
-    r.m_blk = 2 * (u - split * c.num_m_pairs) + static_cast<int>(rank);
+    r.m_blk = 2 * (rr / G) + static_cast<int>(rank);
     r.split = split;
     r.n_lo = split * base + min(split, rem);
     r.n_hi = r.n_lo + base + (split < rem ? 1 : 0);
@@ -675,13 +687,14 @@ template <int MODE>
 __device__ __forceinline__ bool next_unit(const GemmParams& p, const SmemLayout& s, int i, int* u, int role,
                                           uint32_t rank, int lane) {
   if constexpr (is_forward(MODE)) {
-    // role 0: producer, 1: MMA issuer, 2: epilogue warp
-    if (role == 0 && rank == 0) return ring_claim(p, s, i, u);
-    return ring_take(p, s, i, u, role == 2, lane);
-  } else {
-    *u = static_cast<int>(blockIdx.x >> 1) + i * static_cast<int>(gridDim.x >> 1);
-    return true;
+    if (p.dynamic_units) {
+      // role 0: producer, 1: MMA issuer, 2: epilogue warp
+      if (role == 0 && rank == 0) return ring_claim(p, s, i, u);
+      return ring_take(p, s, i, u, role == 2, lane);
+    }
   }
+  *u = static_cast<int>(blockIdx.x >> 1) + i * static_cast<int>(gridDim.x >> 1);
+  return true;
 }
 template <int MODE>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, const Counts& c, const SmemLayout& s,
