@@ -541,14 +541,13 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tm, bool reduce, ui
   ++box_count;
 }
 
-// bf16 tile store (dZ or dH): 4 boxes of 64 columns.  With DZ set, each
-// accumulator value z becomes g (2^(z log2e - lse log2e) - [col == y]), columns
-// at or past V become 0 (the last panel's tail is read back as K by the dH
-// tiles), and box j goes to panel x0 / 64 + j of the dZ block.
-template <bool DZ>
-__device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tcol, int x0, int yrow,
-                                              uint32_t staging0, uint32_t& box_count, int lane, float gt,
-                                              float lse2, int y, int V = 0) {
+// dZ tile store: 4 boxes of 64 columns.  Each accumulator value z becomes
+// g (2^(z log2e - lse log2e) - [col == y]), columns at or past V become 0 (the
+// last panel's tail is read back as K by the dH tiles), and box j goes to
+// panel x0 / 64 + j of the dZ block.
+__device__ __forceinline__ void epi_dz_tile(const CUtensorMap* tm, uint32_t tcol, int x0, int yrow,
+                                            uint32_t staging0, uint32_t& box_count, int lane, float gt, float lse2,
+                                            int y, int V) {
 #pragma unroll 1
   for (int j = 0; j < BN / 64; ++j) {
     uint32_t w[32];
@@ -556,28 +555,26 @@ __device__ __forceinline__ void epi_bf16_tile(const CUtensorMap* tm, uint32_t tc
     for (int h = 0; h < 2; ++h) {
       float v[32];
       tmem_load32_sync(tcol + j * 64 + h * 32, v);
-      if constexpr (DZ) {
-        const int col0 = x0 + j * 64 + h * 32;
+      const int col0 = x0 + j * 64 + h * 32;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = ptx::ex2(fmaf(v[i], kLog2e, -lse2));
-        const int yo = y - col0;
-        if (static_cast<unsigned>(yo) < 32u) {
+      for (int i = 0; i < 32; ++i) v[i] = ptx::ex2(fmaf(v[i], kLog2e, -lse2));
+      const int yo = y - col0;
+      if (static_cast<unsigned>(yo) < 32u) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i == yo) v[i] -= 1.0f;
-        }
+        for (int i = 0; i < 32; ++i)
+          if (i == yo) v[i] -= 1.0f;
+      }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gt;
-        if (col0 + 32 > V) {
+      for (int i = 0; i < 32; ++i) v[i] *= gt;
+      if (col0 + 32 > V) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (col0 + i >= V) v[i] = 0.0f;
-        }
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i >= V) v[i] = 0.0f;
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) w[h * 16 + i] = ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]);
     }
-    store_box(tm, false, staging0, box_count, lane, w, x0 + j * 64, yrow, DZ ? x0 / 64 + j : -1);
+    store_box(tm, false, staging0, box_count, lane, w, x0 + j * 64, yrow, x0 / 64 + j);
   }
 }
 
@@ -841,7 +838,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, const Counts&
             m_run = m_new;
           }
         } else {
-          epi_bf16_tile<true>(&p.tmOut, tcol, nb * BN, un.m_blk * BM + q * 32, staging0, box_count, lane, gt, lse2,
+          epi_dz_tile(&p.tmOut, tcol, nb * BN, un.m_blk * BM + q * 32, staging0, box_count, lane, gt, lse2,
                               y, p.V);
         }
       }
