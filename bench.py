@@ -511,6 +511,11 @@ def run_ours(args):
                   file=sys.stderr, flush=True)
             return 2
         torch.cuda.set_device(local)
+        # NCCL's communicator lines (rank, nRanks, device) go to the log, however the
+        # ranks were started, unless the caller chose NCCL's log level
+        if "NCCL_DEBUG" not in os.environ:
+            os.environ["NCCL_DEBUG"] = "INFO"
+            os.environ.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
