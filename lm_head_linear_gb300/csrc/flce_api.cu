@@ -392,8 +392,9 @@ int pick_split(int64_t m_blocks, int64_t n_blocks, int grid) {
 // The forward's unit schedule: range-major units from the work-index ring when
 // the H blocks of all in-flight token pairs (pairs of them, 512 * Hd bytes each)
 // fit in about 80 MB of L2, else units strided over the pairs with the vocab
-// ranges taken two at a time (when n_split is even).  Both from measurements at
-// Hd = 2048 and 4096 (see the kernel's decode_unit).
+// ranges taken four at a time (two, or one, when n_split does not divide by
+// four).  Both from measurements at Hd = 2048 and 4096 (see the kernel's
+// decode_unit).
 struct FwdSchedule {
   int split_group;
   int dynamic;
@@ -401,7 +402,7 @@ struct FwdSchedule {
 FwdSchedule fwd_schedule(int n_split, int64_t Hd, int64_t pairs) {
   constexpr double kL2Budget = 80.0 * 1024 * 1024;
   if (static_cast<double>(pairs) * 512.0 * static_cast<double>(Hd) <= kL2Budget) return {1, 1};
-  return {n_split % 2 == 0 ? 2 : 1, 0};
+  return {n_split % 4 == 0 ? 4 : (n_split % 2 == 0 ? 2 : 1), 0};
 }
 
 flce_status check_common(const void* H, const void* W, const int64_t* targets, int64_t T, int64_t Hd, int64_t V,

@@ -213,10 +213,11 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const Counts& c
     //    then hold consecutive token pairs of one range and share each W tile
     //    (forward DRAM reads 5.5-7.7 GB at 65,536 x 2048 x 124,160, against
     //    13.5-14.5 GB with G = 2);
-    //  * otherwise G = 2 with the units strided over the pairs (pair c takes
-    //    units c, c + pairs, ...), which puts the two units sharing an H block
+    //  * otherwise G = 4 (or 2) with the units strided over the pairs (pair c
+    //    takes units c, c + pairs, ...), which puts the units sharing an H block
     //    on neighbouring clusters (at 131,072 x 4096 x 124,160 the forward takes
-    //    81 ms so, against 86-90 ms from the ring with G = 1, 2 or 4).
+    //    78-79 ms with G = 4 and 80-81 ms with G = 2, against 86-90 ms from the
+    //    ring with G = 1, 2 or 4).
     const int G = p.split_group;
     const int gsz = G * c.num_m_pairs;
     const int grp = u / gsz;
